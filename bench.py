@@ -1,0 +1,440 @@
+"""Benchmark of the MoE dispatch + combine hot path on GB300.
+
+One step = ep_dispatch_layout + ep_dispatch_nvfp4 (with the fused shared-expert copy) +
+ep_combine over one batch of the DeepSeek-V3-shaped layer: T=4096 tokens, hidden 7168,
+256 routed experts in 8 logical partitions (capacity 4096 tokens each), top-8, one shared
+expert.  Inputs are seeded synthetic (workloads.CONFIGS["dsv3"]), resident in HBM before the
+timed region; L2 is flushed between steps (a 256 MiB write outside the step's events).
+
+Prints one JSON line.  `value` is tokens/s over all ranks (independent replicas, one per GPU:
+the path does not shard), `e2e` the same metric through the C ABI with pinned host buffers
+(host->device inputs and device->host results inside the timed region), `roofline` the
+dominant kernel (combine) against the measured HBM copy bandwidth, `cpu_baseline` the CPU
+oracle on a bounded sample.
+
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "dispatch+combine tokens/s; achieved HBM GB/s vs peak (DSv3-shape MoE layer)"
+UNIT = "tokens/s"
+WORKLOAD = "dsv3"
+FLUSH_BYTES = 256 << 20
+
+
+def workload_config(cfg: W.Config) -> dict:
+    return {"workload": f"{cfg.name}: DeepSeek-V3-like MoE layer, T={cfg.T} tokens, hidden={cfg.H}, "
+                        f"{cfg.E} routed experts in {cfg.P} logical partitions (capacity {cfg.capacity} "
+                        f"tokens), top-{cfg.K}, {'1 fused shared expert' if cfg.S else 'no shared expert'}",
+            "step": "layout + NVFP4 dispatch (2688/rowmax global scale, E2M1 / E4M3 blocks of 16) + combine",
+            "tokens_per_step": cfg.T, "hidden": cfg.H, "n_experts": cfg.E, "top_k": cfg.K,
+            "fused_shared": cfg.S, "n_parts": cfg.P, "capacity": cfg.capacity,
+            "l2": "flushed between steps (256 MiB write, outside the step events)"}
+
+
+def algorithmic_bytes(cfg: W.Config, R: int) -> dict:
+    """Minimum bytes each kernel must move: x read once, every copy written once, every expert
+    row read once, the metadata once."""
+    T, H, K = cfg.T, cfg.H, cfg.K
+    return {
+        "layout": 4 * T * K + 12 * R + 4 * T * K,
+        "dispatch_nvfp4": 2 * T * H + R * (H // 2 + H // 16 + 2),
+        "combine": 2 * R * H + 8 * T * K + 2 * T * H,
+    }
+
+
+def load_peaks() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("ep_common.cuh", "ep_combine.cu"):
+        with open(os.path.join(ROOT, "combine_topk_ids_histogram_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str) -> float | None:
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_dsv3.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+# ------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                                          "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self, t0: float, t1: float) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows, reasons = [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            if self.uuid and self.uuid not in parts[1]:
+                continue
+            try:
+                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm, smax = float(parts[2].split()[0]), float(parts[3].split()[0])
+            except (ValueError, IndexError):
+                continue
+            if t0 - 0.05 <= ts <= t1 + 0.05:
+                rows.append((sm, smax))
+                for n, v in zip(names, parts[6:10]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = sorted(r[0] for r in rows)
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------------------------
+# distributed helpers (independent replicas; only the timing is reduced)
+# ------------------------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(v: float, ws: int, device) -> float:
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------------------------
+# CPU oracle (reported baseline and the reference arm)
+# ------------------------------------------------------------------------------------------
+def oracle_step(oracle, cfg: W.Config, inp: dict, y: np.ndarray, T_s: int) -> None:
+    """The same step on the CPU oracle for the first T_s tokens of the workload."""
+    ids = inp["topk_ids"][:T_s]
+    L = oracle.layout(ids, cfg.E, P=cfg.P, C=cfg.capacity, S=cfg.S)
+    oracle.dispatch_nvfp4(inp["x"][:T_s], L)
+    oracle.combine(y[:L.R_max], inp["probs"][:T_s], L)
+
+
+def time_oracle(cfg: W.Config, inp: dict, y: np.ndarray, budget_s: float, T_s: int | None = None):
+    import oracle
+    oracle.build()
+    if T_s is None:
+        # size the sample from a short probe so it takes about budget_s
+        probe = max(16, cfg.T // 64)
+        t0 = time.perf_counter()
+        oracle_step(oracle, cfg, inp, y, probe)
+        per_tok = (time.perf_counter() - t0) / probe
+        T_s = int(min(cfg.T, max(probe, budget_s / max(per_tok, 1e-9))))
+    reps, t_tot = 0, 0.0
+    while True:
+        t0 = time.perf_counter()
+        oracle_step(oracle, cfg, inp, y, T_s)
+        t_tot += time.perf_counter() - t0
+        reps += 1
+        if t_tot >= budget_s or reps >= 8:
+            break
+    return T_s * reps / t_tot, T_s, reps, t_tot
+
+
+def run_reference(args, cfg):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    inp = W.make_inputs(cfg)
+    y = W.make_expert_out(cfg)
+    steps, warm = args.steps, args.warmup
+    budget_total = 150.0
+    per_step = max(0.05, min(3.0, budget_total / max(1, steps + warm)))
+    import oracle
+    oracle.build()
+    probe = max(16, cfg.T // 64)
+    t0 = time.perf_counter()
+    oracle_step(oracle, cfg, inp, y, probe)
+    per_tok = (time.perf_counter() - t0) / probe
+    T_s = int(min(cfg.T, max(16, per_step / max(per_tok, 1e-9))))
+    for _ in range(warm):
+        oracle_step(oracle, cfg, inp, y, T_s)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_step(oracle, cfg, inp, y, T_s)
+    dt = time.perf_counter() - t0
+    value = T_s * steps / dt
+    sample = (f"first {T_s} of {cfg.T} tokens of the {cfg.name} workload per step (layout over those "
+              f"tokens, NVFP4 dispatch, combine), single-threaded C oracle")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": steps, "warmup": warm, "ms_per_step": dt / steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32/f64", "data": "synthetic",
+            "config": workload_config(cfg),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------
+def run_ours(args, cfg):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    import combine_topk_ids_histogram_gb300 as ep
+
+    inp = W.make_inputs(cfg)
+    y_host = W.make_expert_out(cfg)
+    T, H, E, K, S, P, C = cfg.T, cfg.H, cfg.E, cfg.K, cfg.S, cfg.P, cfg.capacity
+    R_max = W.r_max(cfg)
+
+    def to_dev_bf16(a):
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    x = to_dev_bf16(inp["x"])
+    ids = torch.from_numpy(inp["topk_ids"]).to(dev)
+    probs = torch.from_numpy(inp["probs"]).to(dev)
+    y = to_dev_bf16(y_host)
+    L = ep.Layout(T, K, E, P, bool(S), device=dev)
+    fp4 = torch.empty(R_max, H // 2, dtype=torch.uint8, device=dev)
+    sc = torch.empty(R_max, H // 16, dtype=torch.uint8, device=dev)
+    inv = torch.empty(R_max, dtype=torch.bfloat16, device=dev)
+    so = torch.empty(E + S + 1, dtype=torch.int32, device=dev)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        ep.dispatch_layout(ids, E, P, C, bool(S), out=L, stream=stream)
+        if evs:
+            evs[1].record(stream)
+        ep.dispatch_nvfp4(x, L, out=(fp4, sc, inv, so), stream=stream)
+        if evs:
+            evs[2].record(stream)
+        ep.combine(y, probs, L, out=out, stream=stream)
+        if evs:
+            evs[3].record(stream)
+
+    # correctness of the run itself: no overflow, every row in use
+    step()
+    torch.cuda.synchronize(dev)
+    status = ep.read_status(L)
+    R = int(L.row_offsets[L.G].item())
+    if status != 0:
+        raise RuntimeError(f"layout status {status} on the benchmark workload")
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize(dev)
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    t_host0 = time.time()
+    for i in range(args.steps):
+        flush.fill_(1)
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    t_host1 = time.time()
+    clocks = sampler.stop(t_host0, t_host1) if sampler else None
+
+    per = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3]),
+                     e[0].elapsed_time(e[3])] for e in evs]) * 1e-3     # seconds
+    total = float(per[:, 3].sum())
+    total_max = reduce_max(total, ws, dev)
+    value = ws * T * args.steps / total_max
+    mean = per.mean(axis=0)
+
+    # ---- e2e through the public API with pinned host buffers ----
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    hx = torch.from_numpy(inp["x"].view(np.int16)).pin_memory()
+    hids = torch.from_numpy(inp["topk_ids"]).pin_memory()
+    hprobs = torch.from_numpy(inp["probs"]).pin_memory()
+    hy = torch.from_numpy(y_host.view(np.int16)).pin_memory()
+    ho = {n: torch.empty(t.shape, dtype=t.dtype if t.dtype != torch.bfloat16 else torch.int16).pin_memory()
+          for n, t in (("fp4", fp4), ("sc", sc), ("inv", inv), ("so", so), ("out", out),
+                       ("row_offsets", L.row_offsets), ("expert_ids", L.expert_ids),
+                       ("src_info", L.src_info), ("status", L.status))}
+    xd16 = x.view(torch.int16)
+    yd16 = y.view(torch.int16)
+
+    def e2e_step():
+        xd16.copy_(hx, non_blocking=True)
+        ids.copy_(hids, non_blocking=True)
+        probs.copy_(hprobs, non_blocking=True)
+        yd16.copy_(hy, non_blocking=True)
+        step()
+        for n, t in (("fp4", fp4), ("sc", sc), ("inv", inv.view(torch.int16)), ("so", so),
+                     ("out", out.view(torch.int16)), ("row_offsets", L.row_offsets),
+                     ("expert_ids", L.expert_ids), ("src_info", L.src_info), ("status", L.status)):
+            ho[n].copy_(t, non_blocking=True)
+
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hids, hprobs, hy))
+    d2h = sum(t.numel() * t.element_size() for t in ho.values())
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_t = reduce_max(e0.elapsed_time(e1) * 1e-3, ws, dev)
+    barrier(ws)
+    # the e2e results are the same bytes as the device-resident run
+    if not torch.equal(ho["out"].to(dev), out.view(torch.int16)):
+        raise RuntimeError("e2e output differs from the device-resident step")
+
+    if rank != 0:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+
+    ab = algorithmic_bytes(cfg, R)
+    peak, peak_kind = load_peaks()
+    comb_s = float(mean[2])
+    achieved = ab["combine"] / comb_s / 1e9
+    traffic = recorded_traffic("combine")
+    kernels = {}
+    for j, name in enumerate(("layout", "dispatch_nvfp4", "combine")):
+        gbs = ab[name] / mean[j] / 1e9
+        kernels[name] = {"us": mean[j] * 1e6, "algorithmic_bytes": ab[name], "GB/s": gbs,
+                         "frac_of_measured_peak": gbs / peak}
+    step_bytes = sum(ab.values())
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_max / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded: workloads.CONFIGS['dsv3'])",
+        "config": workload_config(cfg),
+        "roofline": {"kernel": "ep_combine_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": ab["combine"]},
+        "step_roofline": {"algorithmic_bytes": step_bytes, "achieved_GB/s": step_bytes / mean[3] / 1e9,
+                          "frac_of_measured_peak": step_bytes / mean[3] / 1e9 / peak,
+                          "frac_of_8TB/s": step_bytes / mean[3] / 8e12},
+        "kernels": kernels,
+        "e2e": {"value": ws * T * e2e_steps / e2e_t, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "path": "pinned host x/ids/probs/expert outputs -> device, layout + NVFP4 dispatch + "
+                        "combine through the C ABI, dispatched rows + metadata + combined output -> host"},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+        "rows": R,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        v, T_s, reps, secs = time_oracle(cfg, inp, y_host, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"first {T_s} of {T} tokens per step (layout over them, NVFP4 "
+                                          f"dispatch, combine), {reps} step(s), {secs:.1f} s, single thread"}
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=WORKLOAD, choices=sorted(W.CONFIGS))
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    cfg = W.CONFIGS[args.config]
+    if cfg.rerun_C is not None:
+        cfg = W.scaled(cfg, C=cfg.rerun_C)
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,43 @@
+// ep_host.h -- host-side argument checks shared by the entry points of libep_gb300.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "ep.h"
+
+namespace ep {
+
+constexpr int kMaxK = 32;
+constexpr int kMaxE = 1024;
+constexpr int kMaxT = 1 << 24;
+constexpr int kMaxH = 32768;
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Rows every dispatched buffer holds: T*K routed rows plus one shared row per token.
+inline long long rows_max(int T, int K, int S) { return (long long)T * K + (long long)S * T; }
+
+inline bool sizes_ok(int T, int K, int E, int S) {
+    if (T < 0 || T > kMaxT || K < 1 || K > kMaxK || E < K || E > kMaxE) return false;
+    if (S != 0 && S != 1) return false;
+    return rows_max(T, K, S) < (1ll << 31);
+}
+
+// A layout filled by ep_dispatch_layout, with every buffer present.
+inline bool layout_ok(const ep_layout_t *L) {
+    if (!L || !L->row_offsets || !L->row_of || !L->status) return false;
+    if (!sizes_ok(L->T, L->K, L->E, L->fused_shared)) return false;
+    if (L->P < 1 || L->P > L->E || L->E % L->P != 0) return false;
+    return true;
+}
+
+inline bool hidden_ok(int H) { return H >= 16 && H <= kMaxH && H % 16 == 0; }
+
+// Map the result of a launch to a return code.
+inline int launch_result() { return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA; }
+
+}  // namespace ep

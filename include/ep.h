@@ -1,0 +1,221 @@
+/*
+ * ep.h -- C ABI of the GB300 (sm_103a) MoE token dispatch / combine library (libep_gb300.so).
+ *
+ * One GPU, one HBM buffer.  Dispatch turns each token's top-k expert ids into an expert-major
+ * layout and scatters the token rows into it (BF16, or NVFP4 with a per-token global scale);
+ * combine gathers the expert outputs back into token order with the routing probabilities as
+ * weights; the two backward passes are the same operations with the roles swapped.
+ *
+ * Pages this interface follows (cited per entry point by page and section):
+ *   fused_a2a        -- NeMo AutoModel v0.4 API, nemo_automodel.components.moe.megatron.fused_a2a
+ *   token_dispatcher -- NeMo AutoModel v0.7 API, ...components.moe.megatron.token_dispatcher
+ *   Mojo EP dispatch -- Modular MAX API, struct DistributedEPDispatchBlockScaledNVDynGlobalScales
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ * Pointers.  Every tensor argument is a DEVICE pointer into memory the caller allocated (for
+ *   example with PyTorch); the library allocates nothing on these paths and keeps no pointer
+ *   after a call returns.  Tensors are dense and row-major.  bf16 tensors are passed as
+ *   uint16_t (the IEEE bfloat16 bit pattern).  Every tensor pointer must be 16-byte aligned.
+ * Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *   Every call only enqueues work on it and returns; nothing synchronises the host except
+ *   ep_read_status.
+ * Return codes.  An ep_status_t: EP_OK when the work was enqueued.  Host-side argument checks
+ *   run before any CUDA call and return EP_ERR_INVALID_ARG (nothing enqueued); a failed launch
+ *   returns EP_ERR_CUDA.  Conditions only the GPU can see (capacity overflow, expert ids out of
+ *   range) are recorded in the layout's device status word instead, see below.
+ * Sizes.  T tokens, K top-k slots, E routed experts, S = 1 when a shared expert is fused
+ *   (else 0), G = E + S groups, H hidden size, P logical expert partitions, C their capacity.
+ *   R = number of (token, slot) pairs with a valid id + S*T = rows in use, and
+ *   R_max = T*K + S*T = rows every dispatched buffer must be sized for, so that no host
+ *   synchronisation is ever needed to size an output.  Rows [R, R_max) are never written.
+ * Limits.  0 <= T <= 2^24, 1 <= K <= 32, K <= E <= 1024, 1 <= P <= E with E % P == 0,
+ *   C >= 0, T*K + S*T < 2^31; H % 16 == 0 and 16 <= H <= 32768.
+ */
+#ifndef EP_GB300_H
+#define EP_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Host return codes. */
+typedef enum {
+    EP_OK = 0,
+    EP_ERR_INVALID_ARG = 1,   /* an argument failed a host-side check; nothing was enqueued  */
+    EP_ERR_OVERFLOW = 2,      /* ep_read_status: a partition received more than C tokens     */
+    EP_ERR_BAD_EXPERT = 3,    /* ep_read_status: an expert id was outside [-1, E)            */
+    EP_ERR_CUDA = 5           /* a CUDA call failed (launch error, or the sync in read_status) */
+} ep_status_t;
+
+/* Bits of the device status word written by ep_dispatch_layout. */
+#define EP_STATUS_OVERFLOW   1
+#define EP_STATUS_BAD_EXPERT 2
+
+/*
+ * The dispatch layout: caller-allocated device buffers, filled by ep_dispatch_layout and read
+ * by every other entry point.  A layout can be reused for any number of dispatch / combine /
+ * backward calls with the same routing (for example the recompute pass of activation
+ * checkpointing replays a recorded layout without a new layout pass or host read; fused_a2a,
+ * DispatchReplayRecorder / HybridEPDispatchReplayRecorder).
+ *
+ *   row_offsets [G+1]     row_offsets[g] = first row of group g, row_offsets[G] = R
+ *                         (Mojo EP dispatch, execute: row_offsets of the received tokens).
+ *   expert_ids  [R_max]   group of each row, E for the shared expert's rows
+ *                         (Mojo EP dispatch, execute: expert ID of each received token).
+ *   src_info    [R_max*2] (token, slot) of each row, slot K for a shared row
+ *                         (Mojo EP dispatch, execute: originating rank and token index; one
+ *                         GPU, so the rank is always 0 and the slot is kept instead).
+ *   row_of      [T*K]     row of each (token, slot), -1 for an unused slot (the saved mapping
+ *                         combine and the backward passes read; token_dispatcher,
+ *                         _DeepepManager.reversed_mapping_for_combine).
+ *   part_tokens [P]       tokens received by each logical partition.
+ *   status      [1]       EP_STATUS_* bits (token_dispatcher, _assert_no_hybridep_overflow:
+ *                         an overflow flag instead of silent truncation).
+ *   workspace             ep_layout_workspace_bytes(T, K, E, S) bytes of scratch.  It must be
+ *                         zero-filled once before its first use; every call leaves it ready
+ *                         for the next one.  Calls that share a workspace must not overlap on
+ *                         the GPU (use one stream, or one workspace per stream).
+ * The remaining fields are recorded by ep_dispatch_layout and checked by the other calls.
+ */
+typedef struct {
+    int32_t *row_offsets;
+    int32_t *expert_ids;
+    int32_t *src_info;
+    int32_t *row_of;
+    int32_t *part_tokens;
+    int32_t *status;
+    void *workspace;
+    size_t workspace_bytes;
+    int T, K, E, P, capacity, fused_shared;
+} ep_layout_t;
+
+/* Scratch bytes ep_dispatch_layout needs for these sizes (0 on invalid sizes). */
+size_t ep_layout_workspace_bytes(int T, int K, int n_experts, int fused_shared);
+
+/*
+ * ep_dispatch_layout -- the routing metadata of a dispatch.
+ * Defined by: Mojo EP dispatch, execute (route tokens by their top-k ids; row_offsets,
+ * expert_ids, src_info; max_token_per_rank; fused_shared_expert) and fused_a2a,
+ * HybridEPDispatch.forward (topk_idx [tokens, top_k] with -1 for unused slots; dispatched rows
+ * grouped by expert).
+ *
+ *   topk_ids  [T*K] int32 device: expert id of each (token, slot) in [-1, E); -1 = unused.
+ *   n_parts   P logical expert partitions: partition p owns experts [p*E/P, (p+1)*E/P).
+ *   capacity  C: most tokens a partition may receive (a token counts once per partition it
+ *             reaches; the shared expert does not count).
+ *   fused_shared  1: add a group E holding one row per token (slot K), after every routed row.
+ *   L         caller-filled buffer pointers and workspace; the size fields are written here.
+ *
+ * Order: group-major (experts ascending, then the shared group), and inside a group the
+ * (token, slot) pairs in ascending t*K + k order, so the result is deterministic and does not
+ * depend on the launch configuration.
+ * Device-side errors: an id outside [-1, E) sets EP_STATUS_BAD_EXPERT and is treated as unused;
+ * a partition over capacity sets EP_STATUS_OVERFLOW.  The metadata is written in full in both
+ * cases; the status word is rewritten (not OR-ed) by every call.  Every later call that reads
+ * this layout writes none of its outputs while the status word is non-zero: nothing is
+ * silently truncated.
+ */
+int ep_dispatch_layout(const int32_t *topk_ids, int T, int K, int n_experts, int n_parts,
+                       int capacity, int fused_shared, ep_layout_t *L, void *stream);
+
+/*
+ * ep_dispatch_nvfp4 -- scatter every token into its rows as NVFP4.
+ * Defined by: Mojo EP dispatch, execute (each token is quantised to NVFP4 against its own
+ * global scale 2688 / rowmax and sent to its experts; the receiver keeps the BF16 inverse of
+ * that scale per row in output_rowwise_scales; output_scales holds the block scales;
+ * scales_offsets the offsets into the scales buffer).
+ *
+ *   input_tokens           [T*H] bf16.
+ *   out_fp4                [R_max * H/2] uint8: E2M1 codes, element 2j in the low nibble of
+ *                          byte j of the row.
+ *   out_scales             [R_max * H/16] uint8: E4M3 block scale of each 16-element block,
+ *                          row-major, unswizzled.
+ *   out_rowwise_inv_scale  [R_max] bf16: bf16(1/g) per row.
+ *   scales_offsets         [G+1] int32: first scale row of each group (= row_offsets).
+ * Per token, in fp32 with every operation rounded to nearest even: a = max|x|,
+ * g = (a == 0 ? 1 : 2688/a, clamped to FLT_MAX), block scale s = E4M3((blockmax*g)/6),
+ * code = E2M1(x * (g/s)) (0 when s decodes to 0; g/s clamped to FLT_MAX), E4M3 and E2M1
+ * saturating to their largest finite values.  All rows of a token receive identical bytes.
+ */
+int ep_dispatch_nvfp4(const uint16_t *input_tokens, int hidden_size, const ep_layout_t *L,
+                      uint8_t *out_fp4, uint8_t *out_scales, uint16_t *out_rowwise_inv_scale,
+                      int32_t *scales_offsets, void *stream);
+
+/*
+ * ep_dispatch_bf16 -- scatter every token into its rows unchanged.
+ * Defined by: fused_a2a, HybridEPDispatch.forward / hybrid_ep_dispatch (dispatched hidden
+ * states [dispatched_tokens, hidden] grouped by expert).
+ *   input_tokens [T*H] bf16  ->  out [R_max*H] bf16.
+ */
+int ep_dispatch_bf16(const uint16_t *input_tokens, int hidden_size, const ep_layout_t *L,
+                     uint16_t *out, void *stream);
+
+/*
+ * ep_combine -- probability-weighted gather-reduce of the expert outputs into token order.
+ * Defined by: fused_a2a, hybrid_ep_combine / HybridEPCombine.forward (expert outputs
+ * [dispatched_tokens, hidden] -> combined hidden states in the original token order
+ * [tokens, hidden]); token_dispatcher, TokenDispatcherConfig.moe_router_dtype (fp32 router
+ * probabilities weight the expert outputs).
+ *   expert_out [R_max*H] bf16, probs [T*K] fp32  ->  out [T*H] bf16:
+ *   out[t] = bf16( sum over k ascending with row_of[t,k] >= 0 of probs[t,k] * expert_out[row]
+ *                  + (S ? expert_out[row_offsets[E] + t] : 0) ), accumulated in fp32.
+ */
+int ep_combine(const uint16_t *expert_out, const float *probs, int hidden_size,
+               const ep_layout_t *L, uint16_t *out, void *stream);
+
+/*
+ * ep_combine_bwd -- backward of ep_combine.
+ * Defined by: fused_a2a, HybridEPCombine.backward (the combined-output gradient [tokens,
+ * hidden] is dispatched again through the saved layout).
+ *   grad_out [T*H] bf16, expert_out [R_max*H] bf16, probs [T*K] fp32
+ *   -> grad_expert_out [R_max*H] bf16: row of (t,k) = bf16(probs[t,k] * grad_out[t]),
+ *                                      shared row of t = grad_out[t];
+ *   -> grad_probs [T*K] fp32: sum_i grad_out[t,i] * expert_out[row_of[t,k], i] (fp32
+ *      accumulation), 0 for an unused slot.
+ */
+int ep_combine_bwd(const uint16_t *grad_out, const uint16_t *expert_out, const float *probs,
+                   int hidden_size, const ep_layout_t *L, uint16_t *grad_expert_out,
+                   float *grad_probs, void *stream);
+
+/*
+ * ep_dispatch_bwd -- backward of ep_dispatch_bf16 / ep_dispatch_nvfp4 (straight through the
+ * quantiser).
+ * Defined by: fused_a2a, HybridEPDispatch.backward (the dispatched rows' gradients
+ * [dispatched_tokens, hidden] are combined back per token).
+ *   grad_rows [R_max*H] bf16  ->  grad_input [T*H] bf16:
+ *   grad_input[t] = bf16( sum over valid k ascending of grad_rows[row_of[t,k]]
+ *                         + (S ? grad_rows[row_offsets[E] + t] : 0) ), fp32 accumulation.
+ */
+int ep_dispatch_bwd(const uint16_t *grad_rows, int hidden_size, const ep_layout_t *L,
+                    uint16_t *grad_input, void *stream);
+
+/*
+ * ep_read_status -- synchronise `stream` and copy the layout's status word to *host_status.
+ * Returns EP_OK, EP_ERR_OVERFLOW or EP_ERR_BAD_EXPERT (overflow reported first when both bits
+ * are set), or EP_ERR_CUDA.  The one call of this library that blocks the host.
+ */
+int ep_read_status(const ep_layout_t *L, void *stream, int32_t *host_status);
+
+/* Human-readable name of a return code. */
+const char *ep_strerror(int code);
+
+/*
+ * Conversion primitives used by ep_dispatch_nvfp4, exposed so the conversions can be checked
+ * on their own (NVFP4's element and scale formats, Mojo EP dispatch, execute).
+ *   ep_cvt_e2m1: codes[i] = E2M1 code of in[i] (round to nearest even, saturating to +-6,
+ *                sign bit = sign of in[i]), one code per byte in the low nibble.
+ *   ep_cvt_e4m3: codes[i] = E4M3 code of in[i] (round to nearest even, saturating to +-448).
+ *   in [n] fp32 device, codes [n] uint8 device, n >= 0.
+ */
+int ep_cvt_e2m1(const float *in, uint8_t *codes, long n, void *stream);
+int ep_cvt_e4m3(const float *in, uint8_t *codes, long n, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_GB300_H */

@@ -78,6 +78,10 @@ def _declare(L):
     L.oracle_combine_bwd.restype = None
     L.oracle_tiny_expert_outputs.argtypes = [_P, _P, _P, _P, _L, _I, _P]
     L.oracle_tiny_expert_outputs.restype = None
+    L.oracle_e2m1_encode_n.argtypes = [_P, _P, _L]
+    L.oracle_e2m1_encode_n.restype = None
+    L.oracle_e4m3_encode_n.argtypes = [_P, _P, _L]
+    L.oracle_e4m3_encode_n.restype = None
 
 
 def _ptr(a):
@@ -116,15 +120,17 @@ def bf16_to_double(b: int) -> float:
 
 
 def e2m1_encode_array(v: np.ndarray) -> np.ndarray:
-    f = lib().oracle_e2m1_encode
-    return np.fromiter((f(float(x)) for x in np.asarray(v, np.float32).ravel()), np.uint8,
-                       count=np.asarray(v).size).reshape(np.shape(v))
+    a = _c(v, np.float32)
+    out = np.empty(a.shape, np.uint8)
+    lib().oracle_e2m1_encode_n(_ptr(a), _ptr(out), a.size)
+    return out
 
 
 def e4m3_encode_array(v: np.ndarray) -> np.ndarray:
-    f = lib().oracle_e4m3_encode
-    return np.fromiter((f(float(x)) for x in np.asarray(v, np.float32).ravel()), np.uint8,
-                       count=np.asarray(v).size).reshape(np.shape(v))
+    a = _c(v, np.float32)
+    out = np.empty(a.shape, np.uint8)
+    lib().oracle_e4m3_encode_n(_ptr(a), _ptr(out), a.size)
+    return out
 
 
 # ------------------------------------------------------------------------------------------

@@ -443,3 +443,16 @@ void oracle_tiny_expert_outputs(const uint8_t *fp4, const uint8_t *scales, const
         }
     }
 }
+
+/* Array forms of the two encoders (one code per byte), for comparing many values at once. */
+void oracle_e2m1_encode_n(const float *v, uint8_t *codes, long n)
+{
+    for (long i = 0; i < n; i++)
+        codes[i] = oracle_e2m1_encode(v[i]);
+}
+
+void oracle_e4m3_encode_n(const float *v, uint8_t *codes, long n)
+{
+    for (long i = 0; i < n; i++)
+        codes[i] = oracle_e4m3_encode(v[i]);
+}

@@ -1,0 +1,119 @@
+"""Parity at the five workloads' full sizes, in the launch configuration the benchmark times.
+
+The layout is compared in full (the oracle's layout is cheap at any size).  NVFP4 rows and
+combine / backward outputs are compared on sampled tokens (including every outlier and
+all-zero row), each computed by the oracle on a one-token problem built from the full
+workload's inputs.  The large DeepSeek-V3-like microbatch must raise the overflow flag at
+capacity 20000 with every output untouched, then pass in full at capacity 40000."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from gpu_helpers import (abs_dots, assert_close_bf16, assert_close_gradp, check_layout, dev, dev_bf16,
+                         host_bf16, mini_layout_for_token, new_layout)
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+N_SAMPLE = 48
+
+
+@pytest.fixture(scope="module")
+def ep():
+    import combine_topk_ids_histogram_gb300 as ep
+    return ep
+
+
+def sample_tokens(cfg, x, rng):
+    xf = np.abs(W.f32_from_bf16_bits(x[:, :64]))
+    special = np.flatnonzero((xf.max(1) == 0) | (xf.max(1) > 20))[:16]
+    picks = rng.choice(cfg.T, size=N_SAMPLE, replace=False)
+    return np.unique(np.concatenate([special, picks, [0, cfg.T - 1]]))
+
+
+def check_nvfp4_rows(fp4, sc, inv, ref, x, toks, S, E):
+    for t in toks:
+        c, s, i = oracle.nvfp4_quantize_row(x[t])
+        rows = [r for r in ref.row_of[t] if r >= 0] + ([ref.row_offsets[E] + t] if S else [])
+        for r in rows:
+            assert np.array_equal(fp4[r].cpu().numpy(), c), (t, r)
+            assert np.array_equal(sc[r].cpu().numpy(), s), (t, r)
+            assert int(host_bf16(inv[r:r + 1])[0]) == i, (t, r)
+
+
+def check_combine_tokens(out, y_host, probs, ids, ref, toks, E, S, weighted=True):
+    got = host_bf16(out)
+    for t in toks:
+        L1, src = mini_layout_for_token(ref, t, ids[t], E, S)
+        y1 = np.zeros((L1.R_max, y_host.shape[1]), np.uint16)
+        ok = src >= 0
+        y1[ok] = y_host[src[ok]]
+        p1 = probs[t:t + 1] if weighted else None
+        _, r64 = oracle.combine(y1, p1, L1, want64=True)
+        assert_close_bf16(got[t:t + 1], r64, f"token {t}")
+
+
+def run_full(ep, cfg, C=None, backward=False):
+    C = cfg.capacity if C is None else C
+    T, H, E, K, S, P = cfg.T, cfg.H, cfg.E, cfg.K, cfg.S, cfg.P
+    inp = W.make_inputs(cfg)
+    x, ids, probs = inp["x"], inp["topk_ids"], inp["probs"]
+    ref = oracle.layout(ids, E, P=P, C=C, S=S)
+    L = new_layout(ep, T, K, E, P, S)
+    ep.dispatch_layout(dev(ids), E, P, C, bool(S), out=L)
+    check_layout(L, ref, ep)
+    R_max = ref.R_max
+    fp4 = torch.full((R_max, H // 2), 0xA5, dtype=torch.uint8, device="cuda")
+    sc = torch.full((R_max, H // 16), 0xA5, dtype=torch.uint8, device="cuda")
+    inv = torch.full((R_max,), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    so = torch.full((E + S + 1,), -7, dtype=torch.int32, device="cuda")
+    ep.dispatch_nvfp4(dev_bf16(x), L, out=(fp4, sc, inv, so))
+    y_host = W.make_expert_out(cfg)
+    yd = dev_bf16(y_host)
+    out = torch.full((T, H), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    ep.combine(yd, dev(probs), L, out=out)
+    torch.cuda.synchronize()
+    if ref.status:
+        assert (fp4 == 0xA5).all() and (sc == 0xA5).all() and (so == -7).all()
+        assert (inv.view(torch.int16) == -1).all() and (out.view(torch.int16) == -1).all()
+        return ref
+    rng = np.random.default_rng(cfg.index)
+    toks = sample_tokens(cfg, x, rng)
+    assert np.array_equal(so.cpu().numpy(), ref.row_offsets)
+    check_nvfp4_rows(fp4, sc, inv, ref, x, toks, S, E)
+    # rows past R are untouched
+    assert (fp4[ref.R:] == 0xA5).all() and (inv.view(torch.int16)[ref.R:] == -1).all()
+    check_combine_tokens(out, y_host, probs, ids, ref, toks, E, S)
+    if backward:
+        g = W.make_grad_out(cfg)
+        gy, gp = ep.combine_bwd(dev_bf16(g), yd, dev(probs), L)
+        gyh = host_bf16(gy)
+        for t in toks:
+            L1, src = mini_layout_for_token(ref, t, ids[t], E, S)
+            y1 = np.zeros((L1.R_max, H), np.uint16)
+            y1[src >= 0] = y_host[src[src >= 0]]
+            _, rgp, rgy64 = oracle.combine_bwd(g[t:t + 1], y1, probs[t:t + 1], L1, want64=True)
+            for r1 in range(L1.R):
+                assert_close_bf16(gyh[src[r1]][None], rgy64[r1][None], f"grad_y token {t}")
+            assert_close_gradp(gp[t:t + 1].cpu().numpy(), rgp, abs_dots(g[t:t + 1], y1, L1.row_of),
+                               f"grad_p token {t}")
+        gr = W.make_grad_rows(cfg)
+        gx = ep.dispatch_bwd(dev_bf16(gr), L)
+        check_combine_tokens(gx, gr, probs, ids, ref, toks, E, S, weighted=False)
+    return ref
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3", "dsv3", "mixtral"])
+def test_full_size(ep, name):
+    cfg = W.CONFIGS[name]
+    ref = run_full(ep, cfg, backward=(name == "qwen3"))
+    assert ref.status == 0
+
+
+def test_full_size_overflow_then_rerun(ep):
+    cfg = W.CONFIGS["dsv3_large"]
+    ref = run_full(ep, cfg, C=cfg.C)
+    assert ref.status == oracle.OVERFLOW
+    ref = run_full(ep, cfg, C=cfg.rerun_C)
+    assert ref.status == 0

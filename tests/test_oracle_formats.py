@@ -137,3 +137,12 @@ def test_bf16_from_double(v, bits):
 def test_bf16_roundtrip_all_finite_patterns():
     for b in list(range(0, 0x7F80, 7)) + [0x7F7F, 0x0001, 0x8001, 0xFF7F]:
         assert oracle.bf16_from_double(oracle.bf16_to_double(b)) == b
+
+
+def test_array_encoders_match_scalar():
+    rng = np.random.default_rng(3)
+    v = np.concatenate([rng.standard_normal(3000).astype(np.float32) * 4,
+                        np.array([0.0, -0.0, 0.25, 0.75, 5.0, 448.0, 1e-9, -1e30], np.float32)])
+    assert oracle.e2m1_encode_array(v).tolist() == [oracle.e2m1_encode(float(x)) for x in v]
+    w = np.abs(v) * 60
+    assert oracle.e4m3_encode_array(w).tolist() == [oracle.e4m3_encode(float(x)) for x in w]
