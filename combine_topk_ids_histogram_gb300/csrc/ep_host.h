@@ -22,7 +22,7 @@ inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s
 inline long long rows_max(int T, int K, int S) { return (long long)T * K + (long long)S * T; }
 
 inline bool sizes_ok(int T, int K, int E, int S) {
-    if (T < 0 || T > kMaxT || K < 1 || K > kMaxK || E < K || E > kMaxE) return false;
+    if (T < 0 || T > kMaxT || K < 1 || K > kMaxK || E < 1 || E > kMaxE) return false;
     if (S != 0 && S != 1) return false;
     return rows_max(T, K, S) < (1ll << 31);
 }

@@ -29,7 +29,8 @@
  *   R = number of (token, slot) pairs with a valid id + S*T = rows in use, and
  *   R_max = T*K + S*T = rows every dispatched buffer must be sized for, so that no host
  *   synchronisation is ever needed to size an output.  Rows [R, R_max) are never written.
- * Limits.  0 <= T <= 2^24, 1 <= K <= 32, K <= E <= 1024, 1 <= P <= E with E % P == 0,
+ * Limits.  0 <= T <= 2^24, 1 <= K <= 32, 1 <= E <= 1024 (K may exceed E: a token may
+ *   name an expert in several slots), 1 <= P <= E with E % P == 0,
  *   C >= 0, T*K + S*T < 2^31; H % 16 == 0 and 16 <= H <= 32768.
  */
 #ifndef EP_GB300_H

@@ -84,7 +84,7 @@ static double e4m3_mag(int c)
 /* Nearest-even rounding of a >= 0 onto the ascending grid mag(0..top), saturating at top. */
 static int round_to_grid(double a, double (*mag)(int), int top)
 {
-    if (a >= mag(top))
+    if (!(a < mag(top)))   /* saturate; a NaN (outside the method's domain) also stops here */
         return top;
     int c = 0;
     while (!(a < mag(c + 1)))

@@ -57,7 +57,8 @@ def test_host_validation_without_gpu(libpath):
     L = ep.lib()
     bad = ep.EP_ERR_INVALID_ARG
     assert L.ep_layout_workspace_bytes(128, 0, 8, 0) == 0          # K = 0
-    assert L.ep_layout_workspace_bytes(128, 9, 8, 0) == 0          # K > E
+    assert L.ep_layout_workspace_bytes(128, 33, 8, 0) == 0         # K above the limit
+    assert L.ep_layout_workspace_bytes(128, 9, 8, 0) > 0           # K > E: duplicate ids
     assert L.ep_layout_workspace_bytes(128, 2, 2048, 0) == 0       # E above the limit
     assert L.ep_layout_workspace_bytes(-1, 2, 8, 0) == 0
     assert L.ep_layout_workspace_bytes(128, 2, 8, 1) > 0

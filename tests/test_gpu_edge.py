@@ -140,8 +140,9 @@ def test_rows_with_zeros_subnormals_and_outliers(ep):
     x[5, :] = 0
     x[5, 7] = 0x0001                  # smallest subnormal bf16
     x[5, 100] = 0x8002
-    x[6] = W.bf16_bits_from_f32(W.f32_from_bf16_bits(x[6]) * 3e38 / 4)
-    x[7] = W.bf16_bits_from_f32(W.f32_from_bf16_bits(x[7]) * 1e-36)
+    x[6] = W.bf16_bits_from_f32(W.f32_from_bf16_bits(x[6]) * np.float32(7.5e37))   # near the top
+    x[7] = W.bf16_bits_from_f32(W.f32_from_bf16_bits(x[7]) * np.float32(1e-36))    # g clamps
+    assert np.isfinite(W.f32_from_bf16_bits(x)).all()
     x[8, ::16] = 0                    # blocks with a zero element
     x[9, 16:32] = 0x0003              # a block of subnormals next to normal blocks
     full_check(ep, ids, x, p, y, E)

@@ -146,3 +146,10 @@ def test_array_encoders_match_scalar():
     assert oracle.e2m1_encode_array(v).tolist() == [oracle.e2m1_encode(float(x)) for x in v]
     w = np.abs(v) * 60
     assert oracle.e4m3_encode_array(w).tolist() == [oracle.e4m3_encode(float(x)) for x in w]
+
+
+def test_encoders_terminate_outside_the_domain():
+    # NaN is outside the method's domain (never produced from finite inputs); the oracle must
+    # still return instead of searching forever.
+    assert oracle.e2m1_encode(float("nan")) in range(16)
+    assert oracle.e4m3_encode(float("nan")) in range(256)
