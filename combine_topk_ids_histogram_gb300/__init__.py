@@ -24,6 +24,8 @@ EP_ERR_INVALID_ARG = 1
 EP_ERR_OVERFLOW = 2
 EP_ERR_BAD_EXPERT = 3
 EP_ERR_CUDA = 5
+EP_ERR_TOO_LARGE = 6
+NOALLOC_WORKSPACE_BYTES = 1 << 20
 STATUS_OVERFLOW = 1
 STATUS_BAD_EXPERT = 2
 
@@ -60,6 +62,7 @@ _LP = ctypes.POINTER(_Layout)
 SIGNATURES = {
     "ep_layout_workspace_bytes": (_Z, [_I, _I, _I, _I]),
     "ep_dispatch_layout": (_I, [_P, _I, _I, _I, _I, _I, _I, _LP, _P]),
+    "ep_dispatch_layout_noalloc": (_I, [_P, _I, _I, _I, _I, _I, _I, _LP, _P]),
     "ep_dispatch_nvfp4": (_I, [_P, _I, _LP, _P, _P, _P, _P, _P]),
     "ep_dispatch_bf16": (_I, [_P, _I, _LP, _P, _P]),
     "ep_combine": (_I, [_P, _P, _I, _LP, _P, _P]),
@@ -205,6 +208,30 @@ def dispatch_layout(topk_ids: torch.Tensor, n_experts: int, n_parts: int = 1,
                                  int(bool(fused_shared)), L.ref, _stream(stream))
     _check(rc, "ep_dispatch_layout")
     return L
+
+
+def dispatch_layout_noalloc(topk_ids: torch.Tensor, n_experts: int, n_parts: int = 1,
+                            capacity: int | None = None, fused_shared: bool = False,
+                            out: Layout | None = None, stream=None) -> Layout:
+    """ep_dispatch_layout_noalloc: the layout of ``dispatch_layout`` for callers that cannot
+    allocate device memory; its scratch is a fixed 1 MiB array inside the library, so the
+    layout's own workspace is not used.  ``out`` (the output buffers) must be given: this call
+    allocates nothing.  The first call on a device sets the array up (make it before any stream
+    capture); calls that overlap on the GPU race on the shared array."""
+    if topk_ids.dtype != torch.int32 or topk_ids.dim() != 2:
+        raise TypeError("topk_ids must be an int32 [T, K] tensor")
+    if out is None:
+        raise ValueError("dispatch_layout_noalloc writes into caller-provided buffers: pass out=")
+    T, K = topk_ids.shape
+    if (out.T, out.K, out.E, out.P, out.S) != (T, K, n_experts, n_parts, int(bool(fused_shared))):
+        raise ValueError("layout buffers were allocated for other sizes "
+                         f"{(out.T, out.K, out.E, out.P, out.S)}")
+    cap = T if capacity is None else int(capacity)
+    out.capacity = cap
+    rc = _lib.ep_dispatch_layout_noalloc(_ptr(topk_ids) if T > 0 else None, T, K, n_experts, n_parts,
+                                         cap, int(bool(fused_shared)), out.ref, _stream(stream))
+    _check(rc, "ep_dispatch_layout_noalloc")
+    return out
 
 
 def dispatch_nvfp4(x: torch.Tensor, L: Layout, out=None, stream=None):

@@ -368,6 +368,100 @@ extern "C" const char *ep_strerror(int code) {
         case EP_ERR_OVERFLOW: return "a logical partition received more tokens than its capacity";
         case EP_ERR_BAD_EXPERT: return "an expert id was outside [-1, n_experts)";
         case EP_ERR_CUDA: return "CUDA error";
+        case EP_ERR_TOO_LARGE: return "the sizes need more scratch than the fixed no-allocation array holds";
         default: return "unknown error";
     }
+}
+
+// ---------------------------------------------------------------------------------------
+// ep_dispatch_layout_noalloc: the same layout with its scratch in a fixed device array.
+//
+// For callers that must not allocate device memory at all: code running under a framework
+// whose caching allocator owns the whole device, latency-critical paths where an allocation
+// (and the device synchronisation cudaMalloc/cudaFree can imply) is not acceptable, or
+// runtimes that hand a library only its inputs and outputs.  The scratch lives in a
+// file-scope __device__ array of kNoAllocWorkspaceBytes that every GPU which loads this
+// library keeps until the process exits.  Host code cannot use the array's name as a device
+// address (on the host it is only a stand-in symbol), so the device address is looked up once
+// per device with cudaGetSymbolAddress, with that device current, during the first call on
+// that device.  That first call also zeroes the ticket word; every later call leaves it at zero
+// when it finishes.  All calls share the one array, so calls whose work overlaps on the GPU
+// (other streams, other threads) race on it.
+// ---------------------------------------------------------------------------------------
+#include <mutex>
+
+namespace ep {
+namespace {
+
+constexpr size_t kNoAllocWorkspaceBytes = EP_NOALLOC_WORKSPACE_BYTES;
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_workspace[kNoAllocWorkspaceBytes];
+
+std::mutex g_noalloc_mutex;
+void *g_noalloc_address[kNoAllocMaxDevices];   // device address of the array, per device
+
+// Device address of the scratch array on the current device (set up on first use).
+int noalloc_workspace(void **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return EP_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_address[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_workspace) != cudaSuccess || p == nullptr)
+            return EP_ERR_CUDA;
+        if (cudaMemset(p, 0, 256) != cudaSuccess) return EP_ERR_CUDA;   // the ticket starts at 0
+        g_noalloc_address[dev] = p;
+    }
+    *out = g_noalloc_address[dev];
+    return EP_OK;
+}
+
+}  // namespace
+}  // namespace ep
+
+extern "C" int ep_dispatch_layout_noalloc(const int32_t *topk_ids, int T, int K, int n_experts,
+                                          int n_parts, int capacity, int fused_shared,
+                                          ep_layout_t *L, void *stream) {
+    const int E = n_experts, P = n_parts, S = fused_shared;
+    if (!L || !sizes_ok(T, K, E, S)) return EP_ERR_INVALID_ARG;
+    if (P < 1 || P > E || E % P != 0 || capacity < 0) return EP_ERR_INVALID_ARG;
+    if ((T > 0 && !topk_ids) || !L->row_offsets || !L->expert_ids || !L->src_info ||
+        !L->row_of || !L->part_tokens || !L->status)
+        return EP_ERR_INVALID_ARG;
+    const void *ptrs[] = {topk_ids, L->row_offsets, L->expert_ids, L->src_info, L->row_of,
+                          L->part_tokens, L->status};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return EP_ERR_INVALID_ARG;
+    const int tt = tile_tokens(T, K);
+    const int nTiles = num_tiles(T, tt);
+    if (workspace_bytes(nTiles, E) > kNoAllocWorkspaceBytes) return EP_ERR_TOO_LARGE;
+    void *scratch = nullptr;
+    int rc = noalloc_workspace(&scratch);
+    if (rc != EP_OK) return rc;
+
+    L->T = T;
+    L->K = K;
+    L->E = E;
+    L->P = P;
+    L->capacity = capacity;
+    L->fused_shared = S;
+
+    cudaStream_t st = as_stream(stream);
+    Workspace ws = carve(scratch, nTiles, E);
+    size_t smem_count = sizeof(int) * (size_t)max(E + P, kScanChunk + kScanChunk / 32);
+    ep_layout_count_kernel<<<nTiles, kLayoutThreads, smem_count, st>>>(
+        topk_ids, T, K, E, P, capacity, S, tt, nTiles, ws, L->row_offsets, L->part_tokens,
+        L->status);
+    rc = launch_result();
+    if (rc != EP_OK) return rc;
+    size_t smem_rank = sizeof(int) * ((size_t)kLayoutWarps * E + (size_t)tt * K);
+    if (smem_rank > 48 * 1024 &&
+        cudaFuncSetAttribute(ep_layout_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_rank) != cudaSuccess)
+        return EP_ERR_CUDA;
+    ep_layout_rank_kernel<<<nTiles, kLayoutThreads, smem_rank, st>>>(
+        topk_ids, T, K, E, S, tt, nTiles, ws.cnt, L->row_offsets, L->row_of, L->src_info,
+        L->expert_ids);
+    return launch_result();
 }

@@ -49,7 +49,9 @@ typedef enum {
     EP_ERR_INVALID_ARG = 1,   /* an argument failed a host-side check; nothing was enqueued  */
     EP_ERR_OVERFLOW = 2,      /* ep_read_status: a partition received more than C tokens     */
     EP_ERR_BAD_EXPERT = 3,    /* ep_read_status: an expert id was outside [-1, E)            */
-    EP_ERR_CUDA = 5           /* a CUDA call failed (launch error, or the sync in read_status) */
+    EP_ERR_CUDA = 5,          /* a CUDA call failed (launch error, or the sync in read_status) */
+    EP_ERR_TOO_LARGE = 6      /* ep_dispatch_layout_noalloc: the sizes need more scratch than
+                                 its fixed array holds (EP_NOALLOC_WORKSPACE_BYTES)            */
 } ep_status_t;
 
 /* Bits of the device status word written by ep_dispatch_layout. */
@@ -200,6 +202,38 @@ int ep_dispatch_bwd(const uint16_t *grad_rows, int hidden_size, const ep_layout_
  * are set), or EP_ERR_CUDA.  The one call of this library that blocks the host.
  */
 int ep_read_status(const ep_layout_t *L, void *stream, int32_t *host_status);
+
+/*
+ * ep_dispatch_layout_noalloc -- ep_dispatch_layout for callers that cannot allocate device
+ * memory.  The pages have no counterpart of this entry point.
+ *
+ * Some callers cannot call cudaMalloc: code that runs inside a framework whose allocator owns
+ * all device memory, latency-critical paths that must not pay for (or synchronise on) an
+ * allocation, and runtimes that give a library its inputs and outputs and nothing else.  This
+ * entry point computes exactly what ep_dispatch_layout computes, from the same arguments, but
+ * takes its scratch from a fixed array inside the library instead of L->workspace
+ * (L->workspace and L->workspace_bytes are ignored and may be NULL / 0).  The caller still
+ * passes every input and output buffer.
+ *
+ *   Limit: the sizes must satisfy ep_layout_workspace_bytes(T, K, E, S) <=
+ *   EP_NOALLOC_WORKSPACE_BYTES (1 MiB; T = 32768, K = 8, E = 256 needs 131 KiB, and at
+ *   K = 8, E = 256 every T up to 522240 fits); larger sizes return EP_ERR_TOO_LARGE and
+ *   enqueue nothing.  Every GPU that loads the
+ *   library holds that 1 MiB until the process exits.
+ *   Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and zeroes its first 256 bytes with a
+ *   synchronous cudaMemset; make that first call before any stream capture.  Later calls only
+ *   enqueue the two layout kernels.
+ *   Sharing: every call on a device uses the same array, and each call leaves it ready for the
+ *   next.  Calls whose work overlaps on the GPU (two streams, or two host threads) race on the
+ *   array and give undefined results; serialise them.
+ *   No call allocates or frees device memory (no cudaMalloc, cudaFree or allocating library
+ *   routine).  Other errors are those of ep_dispatch_layout.
+ */
+#define EP_NOALLOC_WORKSPACE_BYTES (1u << 20)
+int ep_dispatch_layout_noalloc(const int32_t *topk_ids, int T, int K, int n_experts,
+                               int n_parts, int capacity, int fused_shared, ep_layout_t *L,
+                               void *stream);
 
 /* Human-readable name of a return code. */
 const char *ep_strerror(int code);
