@@ -2,17 +2,19 @@
 // dispatch backward pass with unit weights) and the combine backward pass.
 //
 // Combine follows the fused_a2a page (hybrid_ep_combine / HybridEPCombine.forward: expert
-// outputs back to the original token order, [tokens, hidden]) with the fp32 router
+// outputs brought back to one row per input token, in input order) with the fp32 router
 // probabilities as weights (token_dispatcher page, TokenDispatcherConfig.moe_router_dtype).
 // Its backward follows HybridEPCombine.backward (the output gradient dispatched again through
 // the saved layout) and the dispatch backward follows HybridEPDispatch.backward (row
 // gradients combined back per token).
 //
-// One CTA per token.  Each thread owns 8-element (16-byte) column slices; for a slice it
-// issues the loads of all of the token's K (+1 shared) rows before accumulating, so up to
-// K+1 independent 16-byte loads per thread are in flight.  Accumulation is fp32 with one
-// fused multiply-add per term, in ascending slot order with the shared row last, which makes
-// the result deterministic.
+// Combine runs as many CTAs as fit on the GPU at once, each looping over tokens.  A thread owns
+// 8-element (16-byte) column slices of the token; for a slice it issues the loads of all of
+// the token's K (+1 shared) rows before accumulating, so up to K+1 independent 16-byte loads
+// per thread are in flight, and it already holds the next token's row indices.  The
+// accumulation is fp32 with one fused multiply-add per term, in ascending slot order with the
+// shared row last, which makes the result deterministic.  The backward kernel keeps one CTA
+// per token.
 #include "ep_common.cuh"
 #include "ep_host.h"
 
@@ -21,56 +23,83 @@ namespace {
 
 constexpr int kCombineThreads = 128;
 
+// Persistent: a CTA loops over tokens t = blockIdx.x, blockIdx.x + gridDim.x, ...  While it
+// streams token t's rows it already holds the row indices and weights of its next token, so a
+// token starts with its row loads, never with a metadata round trip.
 template <int KMAX, bool WEIGHTED>
-__global__ void __launch_bounds__(kCombineThreads)
+__global__ void __launch_bounds__(kCombineThreads, KMAX <= 8 ? 9 : 1)
 ep_combine_kernel(const uint16_t *__restrict__ y, const float *__restrict__ probs, int T, int H, int K,
                   int E, int S, int R_max, const int32_t *__restrict__ row_of,
                   const int32_t *__restrict__ row_offsets, const int32_t *__restrict__ status,
                   uint16_t *__restrict__ out) {
-    __shared__ int s_rows[KMAX + 1];
-    __shared__ float s_w[KMAX + 1];
+    __shared__ int s_rows[2][KMAX + 1];
+    __shared__ float s_w[2][KMAX + 1];
+    pdl_begin();
     if (load_status(status)) return;
     const int tid = threadIdx.x;
-    const int t = blockIdx.x;
-    if (tid <= KMAX) {
-        int r = -1;
-        float w = 1.0f;
+    const int shared_base = S ? row_offsets[E] : 0;
+
+    // Slot `tid` (<= KMAX) of token tt: its row (or -1) and weight.
+    auto meta = [&](int tt, int &r, float &w) {
+        r = -1;
+        w = 1.0f;
+        if (tid > KMAX || tt >= T) return;
         if (tid < K) {
-            r = row_of[(size_t)t * K + tid];
-            if (WEIGHTED) w = probs[(size_t)t * K + tid];
+            r = row_of[(size_t)tt * K + tid];
+            if (WEIGHTED) w = probs[(size_t)tt * K + tid];
         } else if (tid == K && S) {
-            r = row_offsets[E] + t;
+            r = shared_base + tt;
         }
-        s_rows[tid] = (r < R_max) ? r : -1;
-        s_w[tid] = w;
+        if (r >= R_max) r = -1;
+    };
+
+    int t = blockIdx.x;
+    {
+        int r;
+        float w;
+        meta(t, r, w);
+        if (tid <= KMAX) {
+            s_rows[0][tid] = r;
+            s_w[0][tid] = w;
+        }
     }
     __syncthreads();
-    int rows[KMAX + 1];
-    float w[KMAX + 1];
-#pragma unroll
-    for (int k = 0; k <= KMAX; ++k) {
-        rows[k] = s_rows[k];
-        w[k] = s_w[k];
-    }
     const int nv = H / 8;
-    for (int c = tid; c < nv; c += blockDim.x) {
-        uint4 d[KMAX + 1];
+    for (int buf = 0; t < T; t += gridDim.x, buf ^= 1) {
+        int r_next;
+        float w_next;
+        meta(t + gridDim.x, r_next, w_next);     // in flight while this token streams
+        // Row indices and weights are re-read from shared memory (broadcasts) for every slice
+        // rather than held in registers, which keeps enough CTAs resident per SM.
+        const int *rows = s_rows[buf];
+        const float *w = s_w[buf];
+        for (int c = tid; c < nv; c += blockDim.x) {
+            uint4 d[KMAX + 1];
 #pragma unroll
-        for (int k = 0; k <= KMAX; ++k)
-            if (rows[k] >= 0) d[k] = ld_stream(y + (size_t)rows[k] * H + (size_t)c * 8);
-        float acc[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-#pragma unroll
-        for (int k = 0; k <= KMAX; ++k) {
-            if (rows[k] >= 0) {
-                float f[8];
-                unpack8(d[k], f);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = fmaf(w[k], f[i], acc[i]);
+            for (int k = 0; k <= KMAX; ++k) {
+                const int r = rows[k];
+                if (r >= 0) d[k] = ld_stream(y + (size_t)r * H + (size_t)c * 8);
             }
+            float acc[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+            for (int k = 0; k <= KMAX; ++k) {
+                if (rows[k] >= 0) {
+                    const float wk = w[k];
+                    float f[8];
+                    unpack8(d[k], f);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i] = fmaf(wk, f[i], acc[i]);
+                }
+            }
+            st_stream(out + (size_t)t * H + (size_t)c * 8, pack8(acc));
         }
-        st_stream(out + (size_t)t * H + (size_t)c * 8, pack8(acc));
+        if (tid <= KMAX) {
+            s_rows[buf ^ 1][tid] = r_next;
+            s_w[buf ^ 1][tid] = w_next;
+        }
+        __syncthreads();
     }
 }
 
@@ -84,6 +113,7 @@ ep_combine_bwd_kernel(const uint16_t *__restrict__ g, const uint16_t *__restrict
     __shared__ int s_rows[KMAX];
     __shared__ float s_p[KMAX];
     __shared__ float s_red[kCombineThreads / 32][KMAX];
+    pdl_begin();
     if (load_status(status)) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int t = blockIdx.x;
@@ -148,24 +178,27 @@ ep_combine_bwd_kernel(const uint16_t *__restrict__ g, const uint16_t *__restrict
     }
 }
 
+template <int KM, bool WEIGHTED>
+int launch_combine_k(const uint16_t *y, const float *probs, int H, const ep_layout_t *L, int R_max,
+                     uint16_t *out, cudaStream_t st) {
+    auto kern = ep_combine_kernel<KM, WEIGHTED>;
+    int grid = resident_blocks(kern, kCombineThreads, 0);
+    if (grid <= 0 || grid > L->T) grid = L->T;
+    return launch_pdl(kern, dim3(grid), dim3(kCombineThreads), 0, st, y, probs, L->T, H, L->K, L->E,
+                      L->fused_shared, R_max, (const int32_t *)L->row_of,
+                      (const int32_t *)L->row_offsets, (const int32_t *)L->status, out);
+}
+
 template <bool WEIGHTED>
 int launch_combine(const uint16_t *y, const float *probs, int H, const ep_layout_t *L,
                    uint16_t *out, cudaStream_t st) {
     const int K = L->K;
     const int R_max = (int)rows_max(L->T, L->K, L->fused_shared);
-    const int threads = kCombineThreads;
-    const dim3 grid(L->T);
-#define EP_COMBINE_CASE(KM)                                                                    \
-    ep_combine_kernel<KM, WEIGHTED><<<grid, threads, 0, st>>>(y, probs, L->T, H, K, L->E,      \
-                                                             L->fused_shared, R_max, L->row_of, \
-                                                             L->row_offsets, L->status, out)
-    if (K <= 2) EP_COMBINE_CASE(2);
-    else if (K <= 4) EP_COMBINE_CASE(4);
-    else if (K <= 8) EP_COMBINE_CASE(8);
-    else if (K <= 16) EP_COMBINE_CASE(16);
-    else EP_COMBINE_CASE(32);
-#undef EP_COMBINE_CASE
-    return launch_result();
+    if (K <= 2) return launch_combine_k<2, WEIGHTED>(y, probs, H, L, R_max, out, st);
+    if (K <= 4) return launch_combine_k<4, WEIGHTED>(y, probs, H, L, R_max, out, st);
+    if (K <= 8) return launch_combine_k<8, WEIGHTED>(y, probs, H, L, R_max, out, st);
+    if (K <= 16) return launch_combine_k<16, WEIGHTED>(y, probs, H, L, R_max, out, st);
+    return launch_combine_k<32, WEIGHTED>(y, probs, H, L, R_max, out, st);
 }
 
 }  // namespace
@@ -211,14 +244,14 @@ extern "C" int ep_combine_bwd(const uint16_t *grad_out, const uint16_t *expert_o
     const int K = L->K;
     const int R_max = (int)rows_max(L->T, L->K, L->fused_shared);
 #define EP_BWD_CASE(KM)                                                                        \
-    ep_combine_bwd_kernel<KM><<<L->T, kCombineThreads, 0, st>>>(                               \
-        grad_out, expert_out, probs, L->T, H, K, L->E, L->fused_shared, R_max, L->row_of,      \
-        L->row_offsets, L->status, grad_expert_out, grad_probs)
+    return launch_pdl(ep_combine_bwd_kernel<KM>, dim3(L->T), dim3(kCombineThreads), 0, st,     \
+                      grad_out, expert_out, probs, L->T, H, K, L->E, L->fused_shared, R_max,   \
+                      (const int32_t *)L->row_of, (const int32_t *)L->row_offsets,             \
+                      (const int32_t *)L->status, grad_expert_out, grad_probs)
     if (K <= 2) EP_BWD_CASE(2);
-    else if (K <= 4) EP_BWD_CASE(4);
-    else if (K <= 8) EP_BWD_CASE(8);
-    else if (K <= 16) EP_BWD_CASE(16);
-    else EP_BWD_CASE(32);
+    if (K <= 4) EP_BWD_CASE(4);
+    if (K <= 8) EP_BWD_CASE(8);
+    if (K <= 16) EP_BWD_CASE(16);
+    EP_BWD_CASE(32);
 #undef EP_BWD_CASE
-    return launch_result();
 }

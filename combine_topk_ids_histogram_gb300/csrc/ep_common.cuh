@@ -19,6 +19,16 @@ constexpr unsigned kFullMask = 0xffffffffu;
 __device__ __forceinline__ uint4 ld_stream(const void *p) { return __ldcs(reinterpret_cast<const uint4 *>(p)); }
 __device__ __forceinline__ void st_stream(void *p, uint4 v) { __stcs(reinterpret_cast<uint4 *>(p), v); }
 
+// Programmatic dependent launch.  Every kernel first waits until the kernel before it in the
+// stream has completed and its memory is visible, and only then lets the next kernel start
+// launching; so a kernel never reads anything before all earlier work in the stream is done,
+// while the next kernel's launch and ramp-up overlap this kernel.  Both are no-ops when the
+// kernel was launched without the programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_begin() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Status word of the layout: read once per CTA; a non-zero word means "write nothing".
 __device__ __forceinline__ int load_status(const int32_t *status) {
     return *reinterpret_cast<const volatile int32_t *>(status);

@@ -47,8 +47,8 @@ __device__ __forceinline__ float absmax8(uint4 v) {
     return m;
 }
 
-template <int BPT>
-__global__ void __launch_bounds__(1024)
+template <int BPT, int MAXT, int MINB>
+__global__ void __launch_bounds__(MAXT, MINB)
 ep_dispatch_nvfp4_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int E, int S, int G, int R_max,
                          const int32_t *__restrict__ row_of, const int32_t *__restrict__ row_offsets,
                          const int32_t *__restrict__ status, uint8_t *__restrict__ out_fp4,
@@ -56,21 +56,14 @@ ep_dispatch_nvfp4_kernel(const uint16_t *__restrict__ x, int T, int H, int K, in
                          int32_t *__restrict__ scales_offsets) {
     __shared__ int s_rows[kMaxRowsPerToken];
     __shared__ float s_red[32];
-    if (load_status(status)) return;
+    pdl_begin();
     const int tid = threadIdx.x;
     const int t = blockIdx.x;
-    if (t == 0)
-        for (int g = tid; g <= G; g += blockDim.x) scales_offsets[g] = row_offsets[g];
-    if (t >= T) return;
-    const int nrows = K + S;
-    if (tid < K) s_rows[tid] = row_of[(size_t)t * K + tid];
-    else if (tid == K && S) s_rows[K] = row_offsets[E] + t;
-
     const int nth = H / (16 * BPT);
-    const bool active = tid < nth;
+    const bool active = tid < nth && t < T;
+    // The token row, the row indices and the status word are all requested before any of them
+    // is used, so a CTA waits for memory once.
     uint4 v[2 * BPT];
-    float bmax[BPT];
-    float tmax = 0.0f;
     if (active) {
         const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H) + (size_t)tid * 2 * BPT;
 #pragma unroll
@@ -79,6 +72,19 @@ ep_dispatch_nvfp4_kernel(const uint16_t *__restrict__ x, int T, int H, int K, in
 #pragma unroll
         for (int i = 0; i < 2 * BPT; ++i) v[i] = make_uint4(0, 0, 0, 0);
     }
+    int my_row = -1;
+    if (t < T) {
+        if (tid < K) my_row = row_of[(size_t)t * K + tid];
+        else if (tid == K && S) my_row = row_offsets[E] + t;
+    }
+    if (load_status(status)) return;
+    if (t == 0)
+        for (int g = tid; g <= G; g += blockDim.x) scales_offsets[g] = row_offsets[g];
+    if (t >= T) return;
+    const int nrows = K + S;
+    if (tid < nrows) s_rows[tid] = my_row;
+    float bmax[BPT];
+    float tmax = 0.0f;
 #pragma unroll
     for (int b = 0; b < BPT; ++b) {
         bmax[b] = fmaxf(absmax8(v[2 * b]), absmax8(v[2 * b + 1]));
@@ -130,6 +136,7 @@ ep_dispatch_bf16_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int
                         const int32_t *__restrict__ row_of, const int32_t *__restrict__ row_offsets,
                         const int32_t *__restrict__ status, uint16_t *__restrict__ out) {
     __shared__ int s_rows[kMaxRowsPerToken];
+    pdl_begin();
     if (load_status(status)) return;
     const int tid = threadIdx.x;
     const int t = blockIdx.x;
@@ -189,15 +196,18 @@ extern "C" int ep_dispatch_nvfp4(const uint16_t *input_tokens, int hidden_size, 
     const int G = L->E + L->fused_shared;
     const int R_max = (int)rows_max(L->T, L->K, L->fused_shared);
     cudaStream_t st = as_stream(stream);
-    if (bpt == 2)
-        ep_dispatch_nvfp4_kernel<2><<<grid, threads, 0, st>>>(
-            input_tokens, L->T, H, L->K, L->E, L->fused_shared, G, R_max, L->row_of, L->row_offsets,
-            L->status, out_fp4, out_scales, out_rowwise_inv_scale, scales_offsets);
-    else
-        ep_dispatch_nvfp4_kernel<1><<<grid, threads, 0, st>>>(
-            input_tokens, L->T, H, L->K, L->E, L->fused_shared, G, R_max, L->row_of, L->row_offsets,
-            L->status, out_fp4, out_scales, out_rowwise_inv_scale, scales_offsets);
-    return launch_result();
+    const int32_t *row_of = L->row_of, *row_offsets = L->row_offsets, *status = L->status;
+#define EP_NVFP4_LAUNCH(BPT, MAXT, MINB)                                                        \
+    return launch_pdl(ep_dispatch_nvfp4_kernel<BPT, MAXT, MINB>, dim3(grid), dim3(threads), 0, st, \
+                      input_tokens, L->T, H, L->K, L->E, L->fused_shared, G, R_max, row_of,     \
+                      row_offsets, status, out_fp4, out_scales, out_rowwise_inv_scale,          \
+                      scales_offsets)
+    // Up to 256 threads (H <= 8192): 5 such CTAs per SM without spilling.
+    if (bpt == 2 && threads <= 256) EP_NVFP4_LAUNCH(2, 256, 5);
+    if (bpt == 2) EP_NVFP4_LAUNCH(2, 1024, 1);
+    if (threads <= 256) EP_NVFP4_LAUNCH(1, 256, 5);
+    EP_NVFP4_LAUNCH(1, 1024, 1);
+#undef EP_NVFP4_LAUNCH
 }
 
 extern "C" int ep_dispatch_bf16(const uint16_t *input_tokens, int hidden_size, const ep_layout_t *L,
@@ -207,10 +217,10 @@ extern "C" int ep_dispatch_bf16(const uint16_t *input_tokens, int hidden_size, c
     if (L->T > 0 && (!input_tokens || !out)) return EP_ERR_INVALID_ARG;
     if ((input_tokens && !aligned16(input_tokens)) || (out && !aligned16(out))) return EP_ERR_INVALID_ARG;
     if (L->T == 0) return EP_OK;
-    ep_dispatch_bf16_kernel<<<L->T, 256, 0, as_stream(stream)>>>(
-        input_tokens, L->T, H, L->K, L->E, L->fused_shared, (int)rows_max(L->T, L->K, L->fused_shared),
-        L->row_of, L->row_offsets, L->status, out);
-    return launch_result();
+    return launch_pdl(ep_dispatch_bf16_kernel, dim3(L->T), dim3(256), 0, as_stream(stream),
+                      input_tokens, L->T, H, L->K, L->E, L->fused_shared,
+                      (int)rows_max(L->T, L->K, L->fused_shared), (const int32_t *)L->row_of,
+                      (const int32_t *)L->row_offsets, (const int32_t *)L->status, out);
 }
 
 extern "C" int ep_cvt_e2m1(const float *in, uint8_t *codes, long n, void *stream) {

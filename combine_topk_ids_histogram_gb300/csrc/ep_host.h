@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "ep.h"
 
 namespace ep {
@@ -39,5 +41,52 @@ inline bool hidden_ok(int H) { return H >= 16 && H <= kMaxH && H % 16 == 0; }
 
 // Map the result of a launch to a return code.
 inline int launch_result() { return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA; }
+inline int launch_result(cudaError_t e) {
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return EP_ERR_CUDA;
+    }
+    return launch_result();
+}
+
+// Launch with programmatic stream serialization, so the kernel's launch overlaps the tail of
+// the previous kernel in the stream (the kernel itself waits for it; see pdl_begin).
+template <typename... KArgs, typename... Args>
+inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                      Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return launch_result(cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...));
+}
+
+// Blocks of `kernel` that fit on the device at once (SM count x resident blocks per SM),
+// for grids that loop over their work.  Cached per device.
+template <typename K>
+inline int resident_blocks(K kernel, int threads, size_t smem) {
+    constexpr int kMaxDev = 64;
+    static int cached[kMaxDev][2];     // (threads, blocks) per device; benign race on first use
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < kMaxDev && cached[dev][0] == threads && cached[dev][1] > 0)
+        return cached[dev][1];
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess)
+        return 0;
+    const int blocks = sms * (per_sm > 0 ? per_sm : 1);
+    if (dev >= 0 && dev < kMaxDev) {
+        cached[dev][1] = blocks;
+        cached[dev][0] = threads;
+    }
+    return blocks;
+}
 
 }  // namespace ep

@@ -4,7 +4,8 @@
 // Follows the Mojo EP dispatch page (DistributedEPDispatchBlockScaledNVDynGlobalScales.execute:
 // route by top-k ids; row_offsets / expert_ids / src_info; max_token_per_rank;
 // atomic_counters coordinating the thread blocks) and the fused_a2a page
-// (HybridEPDispatch.forward: rows grouped by expert, -1 for unused slots).
+// (HybridEPDispatch.forward: the rows come out grouped by expert; an index of -1 routes
+// nowhere).
 //
 // Two launches on the caller's stream:
 //   1. ep_layout_count_kernel: one CTA per tile of tokens builds the tile's expert histogram
@@ -14,8 +15,11 @@
 //      scanned value at (e, j) is the first row of tile j's pairs routed to expert e.  It also
 //      writes row_offsets, part_tokens and the status word, and re-arms the ticket.
 //   2. ep_layout_rank_kernel: one CTA per tile ranks each (t, k) inside its tile and expert,
-//      stably in t*K + k order (warp __match_any_sync plus per-warp prefix counters), and
+//      stably in t*K + k order (equal-id lanes found with one ballot per id bit, plus
+//      per-warp prefix counters), and
 //      writes row_of, src_info and expert_ids; it also writes the shared expert's rows.
+#include <cooperative_groups.h>
+
 #include "ep_common.cuh"
 #include "ep_host.h"
 
@@ -67,6 +71,115 @@ inline Workspace carve(void *base, int nTiles, int E) {
 
 __device__ __forceinline__ bool bad_id(int id, int E) { return id < -1 || id >= E; }
 
+// Lanes of the warp whose key equals this lane's (keys in [0, 2^nbits)): the intersection, over
+// the key's bits, of the lanes that agree with this lane on that bit -- one ballot per bit.
+__device__ __forceinline__ unsigned same_key_lanes(unsigned key, int nbits) {
+    unsigned peers = kFullMask;
+    for (int b = 0; b < nbits; ++b) {
+        const unsigned bit = (key >> b) & 1u;
+        const unsigned m = __ballot_sync(kFullMask, bit);
+        peers &= bit ? m : ~m;
+    }
+    return peers;
+}
+
+// n / d for n < 2^32 / d, from the host-computed magic ceil(2^32 / d): one wide multiply
+// instead of an integer division.
+__device__ __forceinline__ int div_magic(unsigned n, unsigned long long magic) {
+    return (int)(((unsigned long long)n * magic) >> 32);
+}
+inline unsigned long long magic_of(int d) { return ((1ull << 32) + (unsigned)d - 1) / (unsigned)d; }
+
+// Bits needed to hold the values 0 .. n-1.
+inline int key_bits(int n) {
+    int b = 0;
+    while ((1 << b) < n) ++b;
+    return b;
+}
+
+// Adds to s_part[p] the number of the ntok staged tokens (ids in s_ids, K per token, -1 for an
+// unused slot) that reach partition p; a token counts once per partition.  With at most 32
+// partitions each token builds a partition bitmask and each warp adds one ballot count per
+// partition; otherwise each token adds its distinct partitions one by one.
+__device__ __forceinline__ void count_partition_tokens(const int *s_ids, int ntok, int K,
+                                                       unsigned long long per_magic, int P,
+                                                       int *s_part) {
+    const int lane = threadIdx.x & 31;
+    for (int base = 0; base < ntok; base += blockDim.x) {
+        const int tl = base + threadIdx.x;
+        if (P <= 32) {
+            unsigned mask = 0;
+            if (tl < ntok)
+                for (int k = 0; k < K; ++k) {
+                    const int id = s_ids[tl * K + k];
+                    if (id >= 0) mask |= 1u << div_magic((unsigned)id, per_magic);
+                }
+            for (int p = 0; p < P; ++p) {
+                const int c = __popc(__ballot_sync(kFullMask, (mask >> p) & 1u));
+                if (lane == 0 && c) atomicAdd(&s_part[p], c);
+            }
+        } else if (tl < ntok) {
+            for (int k = 0; k < K; ++k) {
+                const int id = s_ids[tl * K + k];
+                if (id < 0) continue;
+                const int p = div_magic((unsigned)id, per_magic);
+                bool first = true;
+                for (int k2 = 0; k2 < k && first; ++k2) {
+                    const int id2 = s_ids[tl * K + k2];
+                    first = !(id2 >= 0 && div_magic((unsigned)id2, per_magic) == p);
+                }
+                if (first) atomicAdd(&s_part[p], 1);
+            }
+        }
+    }
+}
+
+// Stable ranks of one warp's run [w0, w1) of a token range's flat (t, k) indices, the range
+// starting at token t0; hist holds the warp's next row per expert and is advanced.  Writes
+// row_of, src_info and expert_ids.  The (token, slot) of each lane's index is carried from
+// chunk to chunk by adding 32 with a carry, so there is one division per lane, not per id.
+__device__ __forceinline__ void rank_and_write(const int *s_ids, int w0, int w1, int t0, int T, int K,
+                                               int nbits, int *hist, int32_t *row_of,
+                                               int32_t *src_info, int32_t *expert_ids) {
+    const int lane = threadIdx.x & 31;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    int tk = (w0 + lane) / K, kk = (w0 + lane) - tk * K;
+    const int step_t = 32 / K, step_k = 32 - step_t * K;
+    const int limit = T * K;
+    for (int base = w0; base < w1; base += 32) {
+        const int i = base + lane;
+        const int id = i < w1 ? s_ids[i] : -1;
+        const unsigned peers = same_key_lanes((unsigned)(id + 1), nbits);
+        int row = -1;
+        if (id >= 0) row = hist[id] + __popc(peers & lt_mask);
+        __syncwarp();
+        if (id >= 0 && lane == __ffs(peers) - 1) hist[id] += __popc(peers);
+        __syncwarp();
+        if (i < w1) {
+            if (row >= limit) row = -1;   // only a layout raced by a concurrent writer of ids
+            row_of[(size_t)t0 * K + i] = row;
+            if (row >= 0) {
+                reinterpret_cast<int2 *>(src_info)[row] = make_int2(t0 + tk, kk);
+                expert_ids[row] = id;
+            }
+        }
+        tk += step_t;
+        kk += step_k;
+        if (kk >= K) {
+            kk -= K;
+            ++tk;
+        }
+    }
+}
+
+// Dynamic shared memory of the count kernel: histogram, partition counts and the tile's ids,
+// or the last CTA's scan buffer, whichever is larger.
+inline size_t count_smem_bytes(int E, int P, int tt, int K) {
+    const size_t a = (size_t)E + P + (size_t)tt * K;
+    const size_t b = (size_t)kScanChunk + kScanChunk / 32;
+    return sizeof(int) * (a > b ? a : b);
+}
+
 // Exclusive scan of one value per thread across the block (blockDim == kLayoutThreads).
 __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int &total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -92,64 +205,44 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int &t
 
 __global__ void __launch_bounds__(kLayoutThreads)
 ep_layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int P, int C, int S,
-                       int tile_t, int nTiles, Workspace ws, int32_t *__restrict__ row_offsets,
+                       int tile_t, int nTiles, unsigned long long per_magic, Workspace ws, int32_t *__restrict__ row_offsets,
                        int32_t *__restrict__ part_tokens, int32_t *__restrict__ status) {
     extern __shared__ int smem[];
     int *s_hist = smem;          // [E]
     int *s_part = smem + E;      // [P]
+    int *s_ids = smem + E + P;   // [tile_t * K], invalid ids replaced by -1
     __shared__ int s_bad;
     __shared__ int s_last;
     __shared__ int s_warp[kLayoutWarps];
 
+    pdl_begin();
     const int tid = threadIdx.x, lane = tid & 31;
     const int j = blockIdx.x;
-    for (int e = tid; e < E; e += blockDim.x) s_hist[e] = 0;
-    for (int p = tid; p < P; p += blockDim.x) s_part[p] = 0;
-    if (tid == 0) s_bad = 0;
-    __syncthreads();
-
     const int t0 = j * tile_t;
     const int t1 = min(T, t0 + tile_t);
     const int n = max(0, t1 - t0) * K;
     const int32_t *tid_ids = ids + (size_t)t0 * K;
-    // Expert histogram; lanes holding the same id add once through their leader.
-    for (int base = 0; base < n; base += blockDim.x) {
-        int i = base + tid;
-        int id = -1;
-        if (i < n) {
-            id = tid_ids[i];
-            if (bad_id(id, E)) {
-                s_bad = 1;
-                id = -1;
-            }
+    int bad = 0;
+#pragma unroll 8
+    for (int i = tid; i < n; i += blockDim.x) {   // all of a thread's loads in flight together
+        int id = tid_ids[i];
+        if (bad_id(id, E)) {
+            bad = 1;
+            id = -1;
         }
-        unsigned peers = __match_any_sync(kFullMask, id);
-        if (id >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_hist[id], __popc(peers));
+        s_ids[i] = id;
     }
-    // Tokens per partition: a token counts once for every partition one of its ids reaches.
-    const int per = E / P;
-    const int ntok = max(0, t1 - t0);
-    for (int base = 0; base < ntok; base += blockDim.x) {
-        int tl = base + tid;
-        for (int k = 0; k < K; ++k) {
-            int p = -1;
-            if (tl < ntok) {
-                int id = tid_ids[(size_t)tl * K + k];
-                if (!bad_id(id, E) && id >= 0) {
-                    p = id / per;
-                    for (int k2 = 0; k2 < k; ++k2) {
-                        int id2 = tid_ids[(size_t)tl * K + k2];
-                        if (!bad_id(id2, E) && id2 >= 0 && id2 / per == p) {
-                            p = -1;
-                            break;
-                        }
-                    }
-                }
-            }
-            unsigned peers = __match_any_sync(kFullMask, p);
-            if (p >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_part[p], __popc(peers));
-        }
+    for (int e = tid; e < E; e += blockDim.x) s_hist[e] = 0;
+    for (int p = tid; p < P; p += blockDim.x) s_part[p] = 0;
+    bad = __syncthreads_or(bad);
+    if (tid == 0) s_bad = bad;
+
+    // Expert histogram (shared-memory atomics) and tokens per partition.
+    for (int i = tid; i < n; i += blockDim.x) {
+        const int id = s_ids[i];
+        if (id >= 0) atomicAdd(&s_hist[id], 1);
     }
+    count_partition_tokens(s_ids, max(0, t1 - t0), K, per_magic, P, s_part);
     __syncthreads();
     for (int e = tid; e < E; e += blockDim.x) ws.cnt[(size_t)e * nTiles + j] = s_hist[e];
     for (int p = tid; p < P; p += blockDim.x) ws.part[(size_t)p * nTiles + j] = s_part[p];
@@ -164,49 +257,72 @@ ep_layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int
     __threadfence();
 
     // Exclusive scan of cnt in place, kScanChunk entries per pass, through shared memory
-    // (padded by one word per 32 so each thread's contiguous segment is conflict-free).
+    // (padded by one word per 32 so each thread's contiguous segment is conflict-free).  All
+    // of a pass's loads are issued before the first is used, so a pass costs about one L2
+    // round trip instead of one per entry.
     int *s_chunk = smem;   // reuses the histogram space: kScanChunk + kScanChunk/32 ints
     const long total_n = (long)E * nTiles;
-    const int seg = kScanChunk / kLayoutThreads;
+    constexpr int kPer = kScanChunk / kLayoutThreads;
     int carry = 0;
     for (long c0 = 0; c0 < total_n; c0 += kScanChunk) {
         const int len = (int)min((long)kScanChunk, total_n - c0);
-        for (int i = tid; i < len; i += blockDim.x) s_chunk[i + (i >> 5)] = __ldcg(ws.cnt + c0 + i);
+        int v[kPer];
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int i = q * kLayoutThreads + tid;
+            v[q] = i < len ? __ldcg(ws.cnt + c0 + i) : 0;
+        }
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int i = q * kLayoutThreads + tid;
+            s_chunk[i + (i >> 5)] = v[q];
+        }
         __syncthreads();
         int sum = 0;
-        for (int q = 0; q < seg; ++q) {
-            int i = tid * seg + q;
-            if (i < len) sum += s_chunk[i + (i >> 5)];
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int i = tid * kPer + q;
+            sum += s_chunk[i + (i >> 5)];
         }
         int tot;
         int run = carry + block_exclusive_scan(sum, s_warp, tot);
-        for (int q = 0; q < seg; ++q) {
-            int i = tid * seg + q;
-            if (i < len) {
-                int v = s_chunk[i + (i >> 5)];
-                s_chunk[i + (i >> 5)] = run;
-                run += v;
-            }
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int i = tid * kPer + q;
+            const int c = s_chunk[i + (i >> 5)];
+            s_chunk[i + (i >> 5)] = run;
+            run += c;
         }
         __syncthreads();
-        for (int i = tid; i < len; i += blockDim.x) ws.cnt[c0 + i] = s_chunk[i + (i >> 5)];
+        // row_offsets[e] is the scanned value at (e, tile 0).
+        for (int e = tid; e < E; e += blockDim.x) {
+            const long f = (long)e * nTiles - c0;
+            if (f >= 0 && f < len) row_offsets[e] = s_chunk[f + (f >> 5)];
+        }
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int i = q * kLayoutThreads + tid;
+            if (i < len) ws.cnt[c0 + i] = s_chunk[i + (i >> 5)];
+        }
         carry += tot;
         __syncthreads();
     }
-    __threadfence_block();
-    // row_offsets: first row of each expert, then the shared group, then R.
-    for (int e = tid; e < E; e += blockDim.x) row_offsets[e] = __ldcg(ws.cnt + (size_t)e * nTiles);
     if (tid == 0) {
         row_offsets[E] = carry;
         if (S) row_offsets[E + 1] = carry + T;
     }
-    // Partition totals against the capacity, and the bad-id flags.
+    // Partition totals against the capacity (one warp per partition, lanes over the tiles),
+    // and the bad-id flags.
     int flags = 0;
-    for (int p = tid; p < P; p += blockDim.x) {
+    for (int p = tid >> 5; p < P; p += kLayoutWarps) {
         int s = 0;
-        for (int jj = 0; jj < nTiles; ++jj) s += __ldcg(ws.part + (size_t)p * nTiles + jj);
-        part_tokens[p] = s;
-        if (s > C) flags |= EP_STATUS_OVERFLOW;
+#pragma unroll 4
+        for (int jj = lane; jj < nTiles; jj += 32) s += __ldcg(ws.part + (size_t)p * nTiles + jj);
+        s = __reduce_add_sync(kFullMask, s);
+        if (lane == 0) {
+            part_tokens[p] = s;
+            if (s > C) flags |= EP_STATUS_OVERFLOW;
+        }
     }
     for (int jj = tid; jj < nTiles; jj += blockDim.x)
         if (__ldcg(ws.tile_flags + jj)) flags |= EP_STATUS_BAD_EXPERT;
@@ -223,40 +339,50 @@ ep_layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int
 
 __global__ void __launch_bounds__(kLayoutThreads)
 ep_layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int S, int tile_t,
-                      int nTiles, const int32_t *__restrict__ cnt,
+                      int nTiles, int nbits, const int32_t *__restrict__ cnt,
                       const int32_t *__restrict__ row_offsets, int32_t *__restrict__ row_of,
                       int32_t *__restrict__ src_info, int32_t *__restrict__ expert_ids) {
     extern __shared__ int smem[];
     int *s_whist = smem;                       // [kLayoutWarps][E]
     int *s_ids = smem + kLayoutWarps * E;      // [tile_t * K]
+    pdl_begin();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int j = blockIdx.x;
     const int t0 = j * tile_t;
     const int t1 = min(T, t0 + tile_t);
     const int n = max(0, t1 - t0) * K;
 
-    for (int i = tid; i < kLayoutWarps * E; i += blockDim.x) s_whist[i] = 0;
+    // The tile's scanned bases (one per expert), loaded before they are needed.
+    constexpr int kMaxEPerThread = kMaxE / kLayoutThreads;
+    int base_e[kMaxEPerThread];
+#pragma unroll
+    for (int q = 0; q < kMaxEPerThread; ++q) {
+        const int e = tid + q * kLayoutThreads;
+        base_e[q] = e < E ? cnt[(size_t)e * nTiles + j] : 0;
+    }
+#pragma unroll 8
     for (int i = tid; i < n; i += blockDim.x) {
         int id = ids[(size_t)t0 * K + i];
         s_ids[i] = bad_id(id, E) ? -1 : id;
     }
+    for (int i = tid; i < kLayoutWarps * E; i += blockDim.x) s_whist[i] = 0;
     __syncthreads();
 
     // Each warp owns one contiguous run of the tile's flat (t, k) indices.
     const int per_warp = ((n + kLayoutWarps - 1) / kLayoutWarps + 31) / 32 * 32;
     const int w0 = min(n, warp * per_warp), w1 = min(n, w0 + per_warp);
     int *hist = s_whist + warp * E;
-    for (int base = w0; base < w1; base += 32) {
-        int i = base + lane;
-        int id = i < w1 ? s_ids[i] : -1;
-        unsigned peers = __match_any_sync(kFullMask, id);
-        if (id >= 0 && lane == __ffs(peers) - 1) hist[id] += __popc(peers);
-        __syncwarp();
+    for (int i = w0 + lane; i < w1; i += 32) {
+        const int id = s_ids[i];
+        if (id >= 0) atomicAdd(&hist[id], 1);
     }
     __syncthreads();
     // First row of each (warp, expert): the tile's scanned base plus earlier warps' counts.
-    for (int e = tid; e < E; e += blockDim.x) {
-        int run = cnt[(size_t)e * nTiles + j];
+#pragma unroll
+    for (int q = 0; q < kMaxEPerThread; ++q) {
+        const int e = tid + q * kLayoutThreads;
+        if (e >= E) break;
+        int run = base_e[q];
         for (int w = 0; w < kLayoutWarps; ++w) {
             int c = s_whist[w * E + e];
             s_whist[w * E + e] = run;
@@ -264,27 +390,7 @@ ep_layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int 
         }
     }
     __syncthreads();
-    const unsigned lt_mask = (1u << lane) - 1u;
-    for (int base = w0; base < w1; base += 32) {
-        int i = base + lane;
-        int id = i < w1 ? s_ids[i] : -1;
-        unsigned peers = __match_any_sync(kFullMask, id);
-        int row = -1;
-        if (id >= 0) row = hist[id] + __popc(peers & lt_mask);
-        __syncwarp();
-        if (id >= 0 && lane == __ffs(peers) - 1) hist[id] += __popc(peers);
-        __syncwarp();
-        if (i < w1) {
-            size_t flat = (size_t)t0 * K + i;
-            if (row >= T * K) row = -1;   // only a layout raced by a concurrent writer of ids
-            row_of[flat] = row;
-            if (row >= 0) {
-                int t = t0 + i / K;
-                reinterpret_cast<int2 *>(src_info)[row] = make_int2(t, i - (i / K) * K);
-                expert_ids[row] = id;
-            }
-        }
-    }
+    rank_and_write(s_ids, w0, w1, t0, T, K, nbits, hist, row_of, src_info, expert_ids);
     if (S) {
         const int rs = row_offsets[E];
         for (int t = t0 + tid; t < t1; t += blockDim.x) {
@@ -292,6 +398,376 @@ ep_layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int 
             expert_ids[rs + t] = E;
         }
     }
+}
+
+// ---------------------------------------------------------------------------------------
+// Single-cluster layout.  When one thread-block cluster can hold every id, the whole layout is
+// one kernel on a cluster of up to 16 CTAs, each on its own SM and each owning a contiguous range
+// of tokens.  Per CTA:
+//   A. load the range's ids into shared memory (bad ids become -1; with at most 32 partitions a
+//      per-token partition bitmask is built on the way), per-warp expert histograms;
+//   B. one warp per expert group scans the per-warp counts (shuffles), giving each warp's first
+//      local row per expert and the CTA's count per expert; partition token counts from the
+//      bitmasks (one ballot per partition);
+//   C. each CTA pushes its expert counts into every CTA's shared memory, and its partition
+//      counts and bad-id flag into CTA 0's, through distributed shared memory; one cluster
+//      barrier; from then on every read is local: cluster totals -> row_offsets (a block scan),
+//      counts of the CTAs before this one -> this CTA's first row per expert;
+//   D. stable ranks (equal-id lanes by ballots), row_of in flat order, and each routed row staged
+//      in shared memory in expert order, so src_info and expert_ids go out as contiguous runs.
+// One launch, one cluster barrier after start-up, no global scratch, atomics or fences.
+// ---------------------------------------------------------------------------------------
+constexpr int kClThreads = 1024;
+constexpr int kClWarps = kClThreads / 32;
+constexpr int kClMaxCtas = 16;            // largest cluster (non-portable; 8 where 16 is refused)
+constexpr int kClMaxIds = 8192;           // ids of one CTA's range held in shared memory
+constexpr int kClIdsPerCta = 2048;        // below this many ids per CTA, use fewer CTAs
+constexpr int kClExpertsPerThread = kMaxE / kClThreads;
+constexpr size_t kClMaxSmem = 216 * 1024;   // dynamic; leaves room for the static arrays
+
+// Shared-memory plan of the cluster kernel (ints): per-expert arrays, the pushed counts of every
+// CTA, partition counts pushed to CTA 0, per-warp histograms, the ids, the staging area and the
+// per-token partition masks.
+struct ClusterSmem {
+    int hist, first, locoff, all, part_all, bad_all, whist, ids, stage, tokmask, total;
+};
+__host__ __device__ inline ClusterSmem cluster_smem_plan(int E, int P, int tile_t, int K) {
+    ClusterSmem m;
+    int o = 0;
+    m.hist = o; o += E;
+    m.first = o; o += E;
+    m.locoff = o; o += E;
+    m.all = o; o += kClMaxCtas * E;
+    m.part_all = o; o += kClMaxCtas * P;
+    m.bad_all = o; o += kClMaxCtas;
+    m.whist = o; o += kClWarps * (E + 1);   // rows padded to E + 1: conflict-free scans
+    m.ids = o; o += tile_t * K;
+    m.stage = o; o += tile_t * K;
+    m.tokmask = o; o += tile_t;
+    m.total = o;
+    return m;
+}
+inline size_t cluster_smem_bytes(int E, int P, int tile_t, int K) {
+    return sizeof(int) * (size_t)cluster_smem_plan(E, P, tile_t, K).total;
+}
+
+// CTAs of the single-cluster layout for these sizes (at most max_ctas), or 0 when it cannot
+// hold them.
+inline int cluster_ctas(int T, int K, int E, int P, int max_ctas) {
+    const long n = (long)T * K;
+    long c = (n + kClIdsPerCta - 1) / kClIdsPerCta;
+    if (c < 1) c = 1;
+    if (c > max_ctas) c = max_ctas;
+    const long per = (T + c - 1) / c;
+    if (per * K > kClMaxIds) return 0;
+    if (cluster_smem_bytes(E, P, (int)per, K) > kClMaxSmem) return 0;
+    return (int)c;
+}
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kClThreads, 1)
+ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int P, int C, int S,
+                         int tile_t, int nbits, unsigned long long per_magic,
+                         unsigned long long k_magic, int32_t *__restrict__ row_offsets,
+                         int32_t *__restrict__ expert_ids, int32_t *__restrict__ src_info,
+                         int32_t *__restrict__ row_of, int32_t *__restrict__ part_tokens,
+                         int32_t *__restrict__ status) {
+    extern __shared__ int smem[];
+    const ClusterSmem m = cluster_smem_plan(E, P, tile_t, K);
+    int *s_hist = smem + m.hist, *s_first = smem + m.first, *s_locoff = smem + m.locoff;
+    int *s_all = smem + m.all, *s_part_all = smem + m.part_all, *s_bad_all = smem + m.bad_all;
+    int *s_whist = smem + m.whist, *s_ids = smem + m.ids, *s_stage = smem + m.stage;
+    int *s_tokmask = smem + m.tokmask;
+    __shared__ int s_warp[kClWarps];
+    __shared__ int s_warp2[kClWarps];
+    __shared__ int s_bad;
+
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int crank = (int)cluster.block_rank();
+    const int ncta = (int)cluster.num_blocks();
+    cluster_arrive_relaxed();   // "this CTA has started"; waited on before the first remote write
+    pdl_begin();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int t0 = crank * tile_t;
+    const int t1 = min(T, t0 + tile_t);
+    const int ntok = max(0, t1 - t0);
+    const int n = ntok * K;
+    const bool masks = P <= 32;
+
+    // A. ids, per-token partition masks, per-warp histograms (row stride E + 1)
+    const int EP = E + 1;
+    for (int i = tid; i < kClWarps * EP; i += kClThreads) s_whist[i] = 0;
+    if (masks)
+        for (int i = tid; i < ntok; i += kClThreads) s_tokmask[i] = 0;
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+    const int per_warp = ((n + kClWarps - 1) / kClWarps + 31) / 32 * 32;
+    const int w0 = min(n, warp * per_warp), w1 = min(n, w0 + per_warp);
+    int *hist = s_whist + warp * EP;
+    {
+        int bad = 0;
+        // the warp's own run, so its histogram needs no second pass over shared memory
+        int tk = (w0 + lane) / K, kk = (w0 + lane) - tk * K;
+        const int step_t = 32 / K, step_k = 32 - step_t * K;
+        for (int i = w0 + lane; i < w1; i += 32) {
+            int id = ids[(size_t)t0 * K + i];
+            if (bad_id(id, E)) {
+                bad = 1;
+                id = -1;
+            }
+            s_ids[i] = id;
+            if (id >= 0) {
+                atomicAdd(&hist[id], 1);
+                if (masks) atomicOr(&s_tokmask[tk], (int)(1u << div_magic((unsigned)id, per_magic)));
+            }
+            tk += step_t;
+            kk += step_k;
+            if (kk >= K) {
+                kk -= K;
+                ++tk;
+            }
+        }
+        if (bad) s_bad = 1;
+    }
+    if (!masks)
+        for (int p = tid; p < P; p += kClThreads) s_part_all[crank * P + p] = 0;   // local scratch row
+    __syncthreads();
+
+    // B. per-(warp, expert) exclusive prefix over the warps, and the CTA's count per expert:
+    //    warp w scans experts w, w + 32, ...; lane l holds warp l's count.
+    for (int e = warp; e < E; e += kClWarps) {
+        const int c = s_whist[lane * EP + e];
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(kFullMask, incl, o);
+            if (lane >= o) incl += v;
+        }
+        s_whist[lane * EP + e] = incl - c;
+        if (lane == 31) s_hist[e] = incl;
+    }
+    //    tokens per partition: warp w counts partitions w, w + 32, ... from the token masks
+    if (masks) {
+        for (int p = warp; p < P; p += kClWarps) {
+            int c = 0;
+            for (int tl = lane; tl < ntok; tl += 32) c += (s_tokmask[tl] >> p) & 1;
+            c = __reduce_add_sync(kFullMask, c);
+            if (lane == 0) s_part_all[crank * P + p] = c;
+        }
+    } else {
+        count_partition_tokens(s_ids, ntok, K, per_magic, P, s_part_all + crank * P);
+    }
+    __syncthreads();
+
+    // C. push this CTA's counts through distributed shared memory, then one cluster barrier
+    cluster_wait();   // every CTA of the cluster has started
+    for (int idx = tid; idx < ncta * E; idx += kClThreads) {
+        const int r = idx / E, e = idx - r * E;
+        cluster.map_shared_rank(s_all, r)[crank * E + e] = s_hist[e];
+    }
+    if (crank != 0) {
+        int *rp = cluster.map_shared_rank(s_part_all, 0);
+        for (int p = tid; p < P; p += kClThreads) rp[crank * P + p] = s_part_all[crank * P + p];
+    }
+    if (tid == 0) cluster.map_shared_rank(s_bad_all, 0)[crank] = s_bad;
+    cluster_sync_all();
+
+    //    cluster totals per expert (thread tid owns experts kClExpertsPerThread*tid + q)
+    int mine = 0, mine_local = 0;
+    int before[kClExpertsPerThread], total[kClExpertsPerThread];
+#pragma unroll
+    for (int q = 0; q < kClExpertsPerThread; ++q) {
+        const int e = kClExpertsPerThread * tid + q;
+        before[q] = 0;
+        total[q] = 0;
+        if (e < E) {
+#pragma unroll
+            for (int r = 0; r < kClMaxCtas; ++r) {
+                if (r < ncta) {
+                    const int v = s_all[r * E + e];
+                    if (r < crank) before[q] += v;
+                    total[q] += v;
+                }
+            }
+            mine_local += s_hist[e];
+        }
+        mine += total[q];
+    }
+    int incl = mine, incl_l = mine_local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(kFullMask, incl, o);
+        const int vl = __shfl_up_sync(kFullMask, incl_l, o);
+        if (lane >= o) {
+            incl += v;
+            incl_l += vl;
+        }
+    }
+    if (lane == 31) {
+        s_warp[warp] = incl;
+        s_warp2[warp] = incl_l;
+    }
+    int over = 0, any_bad = 0;
+    if (crank == 0) {
+        for (int p = tid; p < P; p += kClThreads) {
+            int c = 0;
+            for (int r = 0; r < ncta; ++r) c += s_part_all[r * P + p];
+            part_tokens[p] = c;
+            if (c > C) over = 1;
+        }
+        if (tid < ncta && s_bad_all[tid]) any_bad = 1;
+    }
+    // __syncthreads_or returns a predicate, so each status bit is reduced on its own; the
+    // barrier also publishes s_warp / s_warp2.
+    over = __syncthreads_or(over);
+    any_bad = __syncthreads_or(any_bad);
+    const int flags = (over ? EP_STATUS_OVERFLOW : 0) | (any_bad ? EP_STATUS_BAD_EXPERT : 0);
+    int routed = 0, warp_before = 0, warp_before_l = 0, n_valid = 0;
+    for (int w = 0; w < kClWarps; ++w) {
+        if (w < warp) {
+            warp_before += s_warp[w];
+            warp_before_l += s_warp2[w];
+        }
+        routed += s_warp[w];
+        n_valid += s_warp2[w];
+    }
+    int excl = warp_before + incl - mine;
+    int excl_l = warp_before_l + incl_l - mine_local;
+#pragma unroll
+    for (int q = 0; q < kClExpertsPerThread; ++q) {
+        const int e = kClExpertsPerThread * tid + q;
+        if (e < E) {
+            if (crank == 0) row_offsets[e] = excl;
+            s_first[e] = excl + before[q];
+            s_locoff[e] = excl_l;
+            excl_l += s_hist[e];
+        }
+        excl += total[q];
+    }
+    if (crank == 0 && tid == 0) {
+        row_offsets[E] = routed;
+        if (S) row_offsets[E + 1] = routed + T;
+        *status = flags;
+    }
+    __syncthreads();
+
+    // D. stable ranks: row_of in flat order; each routed (t, k) staged at its expert-ordered
+    //    local position (flat index in the low bits, expert in the high bits).
+    {
+        const unsigned lt_mask = (1u << lane) - 1u;
+        const int limit = T * K;
+        for (int base = w0; base < w1; base += 32) {
+            const int i = base + lane;
+            const int id = i < w1 ? s_ids[i] : -1;
+            const unsigned peers = same_key_lanes((unsigned)(id + 1), nbits);
+            int local = -1;
+            if (id >= 0) local = hist[id] + __popc(peers & lt_mask);
+            __syncwarp();
+            if (id >= 0 && lane == __ffs(peers) - 1) hist[id] += __popc(peers);
+            __syncwarp();
+            if (i < w1) {
+                int row = -1;
+                if (id >= 0) {
+                    row = s_first[id] + local;
+                    if (row >= limit) row = -1;
+                    else s_stage[s_locoff[id] + local] = (id << 16) | i;
+                }
+                row_of[(size_t)t0 * K + i] = row;
+            }
+        }
+    }
+    __syncthreads();
+    for (int j = tid; j < n_valid; j += kClThreads) {
+        const int v = s_stage[j];
+        const int e = v >> 16, i = v & 0xffff;
+        if (e < 0 || e >= E || i >= n) continue;   // only a layout raced by a writer of ids
+        const int row = s_first[e] + (j - s_locoff[e]);
+        if (row < 0 || row >= T * K) continue;
+        const int tk = div_magic((unsigned)i, k_magic);
+        reinterpret_cast<int2 *>(src_info)[row] = make_int2(t0 + tk, i - tk * K);
+        expert_ids[row] = e;
+    }
+    if (S) {
+        for (int t = t0 + tid; t < t1; t += kClThreads) {
+            reinterpret_cast<int2 *>(src_info)[routed + t] = make_int2(t, K);
+            expert_ids[routed + t] = E;
+        }
+    }
+}
+
+// Largest cluster the device runs for the layout kernel: 16 CTAs where the non-portable size is
+// granted, else 8 (the portable size).  Looked up once per device.
+inline int max_cluster_ctas() {
+    constexpr int kMaxDev = 64;
+    static int cached[kMaxDev];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 8;
+    if (dev >= 0 && dev < kMaxDev && cached[dev]) return cached[dev];
+    int best = 8;
+    if (cudaFuncSetAttribute(ep_layout_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kClMaxSmem) == cudaSuccess &&
+        cudaFuncSetAttribute(ep_layout_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                             1) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(16);
+        cfg.blockDim = dim3(kClThreads);
+        cfg.dynamicSmemBytes = kClMaxSmem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 16;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, ep_layout_cluster_kernel, &cfg) == cudaSuccess && n > 0)
+            best = 16;
+    }
+    (void)cudaGetLastError();
+    if (dev >= 0 && dev < kMaxDev) cached[dev] = best;
+    return best;
+}
+
+// The whole layout as one cluster of CTAs (see ep_layout_cluster_kernel).  Returns -1 when the
+// sizes do not fit one cluster (the caller then uses the two-kernel path).
+inline int launch_cluster_layout(const int32_t *ids, int T, int K, int E, int P, int C, int S,
+                                 ep_layout_t *L, cudaStream_t st) {
+    const int ncta = cluster_ctas(T, K, E, P, max_cluster_ctas());
+    if (ncta == 0) return -1;
+    const int tile_t = (T + ncta - 1) / ncta;
+    const size_t smem = cluster_smem_bytes(E, P, tile_t, K);
+    if (cudaFuncSetAttribute(ep_layout_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kClMaxSmem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return -1;   // the two-kernel path needs no such opt-in
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ncta);
+    cfg.blockDim = dim3(kClThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ncta;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return launch_result(cudaLaunchKernelEx(&cfg, ep_layout_cluster_kernel, ids, T, K, E, P, C, S,
+                                            tile_t, key_bits(E + 1), magic_of(E / P), magic_of(K),
+                                            L->row_offsets, L->expert_ids, L->src_info, L->row_of,
+                                            L->part_tokens, L->status));
 }
 
 }  // namespace
@@ -330,22 +806,23 @@ extern "C" int ep_dispatch_layout(const int32_t *topk_ids, int T, int K, int n_e
     L->fused_shared = S;
 
     cudaStream_t st = as_stream(stream);
+    const int rc_cl = launch_cluster_layout(topk_ids, T, K, E, P, capacity, S, L, st);
+    if (rc_cl != -1) return rc_cl;
     Workspace ws = carve(L->workspace, nTiles, E);
-    size_t smem_count = sizeof(int) * (size_t)max(E + P, kScanChunk + kScanChunk / 32);
-    ep_layout_count_kernel<<<nTiles, kLayoutThreads, smem_count, st>>>(
-        topk_ids, T, K, E, P, capacity, S, tt, nTiles, ws, L->row_offsets, L->part_tokens,
-        L->status);
-    int rc = launch_result();
+    const size_t smem_count = count_smem_bytes(E, P, tt, K);
+    int rc = launch_pdl(ep_layout_count_kernel, dim3(nTiles), dim3(kLayoutThreads), smem_count, st,
+                        topk_ids, T, K, E, P, capacity, S, tt, nTiles, magic_of(E / P), ws,
+                        L->row_offsets,
+                        L->part_tokens, L->status);
     if (rc != EP_OK) return rc;
     size_t smem_rank = sizeof(int) * ((size_t)kLayoutWarps * E + (size_t)tt * K);
     if (smem_rank > 48 * 1024 &&
         cudaFuncSetAttribute(ep_layout_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem_rank) != cudaSuccess)
         return EP_ERR_CUDA;
-    ep_layout_rank_kernel<<<nTiles, kLayoutThreads, smem_rank, st>>>(
-        topk_ids, T, K, E, S, tt, nTiles, ws.cnt, L->row_offsets, L->row_of, L->src_info,
-        L->expert_ids);
-    return launch_result();
+    return launch_pdl(ep_layout_rank_kernel, dim3(nTiles), dim3(kLayoutThreads), smem_rank, st,
+                      topk_ids, T, K, E, S, tt, nTiles, key_bits(E + 1), (const int32_t *)ws.cnt,
+                      (const int32_t *)L->row_offsets, L->row_of, L->src_info, L->expert_ids);
 }
 
 extern "C" int ep_read_status(const ep_layout_t *L, void *stream, int32_t *host_status) {
@@ -449,9 +926,9 @@ extern "C" int ep_dispatch_layout_noalloc(const int32_t *topk_ids, int T, int K,
 
     cudaStream_t st = as_stream(stream);
     Workspace ws = carve(scratch, nTiles, E);
-    size_t smem_count = sizeof(int) * (size_t)max(E + P, kScanChunk + kScanChunk / 32);
+    const size_t smem_count = count_smem_bytes(E, P, tt, K);
     ep_layout_count_kernel<<<nTiles, kLayoutThreads, smem_count, st>>>(
-        topk_ids, T, K, E, P, capacity, S, tt, nTiles, ws, L->row_offsets, L->part_tokens,
+        topk_ids, T, K, E, P, capacity, S, tt, nTiles, magic_of(E / P), ws, L->row_offsets, L->part_tokens,
         L->status);
     rc = launch_result();
     if (rc != EP_OK) return rc;
@@ -461,7 +938,7 @@ extern "C" int ep_dispatch_layout_noalloc(const int32_t *topk_ids, int T, int K,
                              (int)smem_rank) != cudaSuccess)
         return EP_ERR_CUDA;
     ep_layout_rank_kernel<<<nTiles, kLayoutThreads, smem_rank, st>>>(
-        topk_ids, T, K, E, S, tt, nTiles, ws.cnt, L->row_offsets, L->row_of, L->src_info,
+        topk_ids, T, K, E, S, tt, nTiles, key_bits(E + 1), ws.cnt, L->row_offsets, L->row_of, L->src_info,
         L->expert_ids);
     return launch_result();
 }

@@ -103,8 +103,8 @@ size_t ep_layout_workspace_bytes(int T, int K, int n_experts, int fused_shared);
  * ep_dispatch_layout -- the routing metadata of a dispatch.
  * Defined by: Mojo EP dispatch, execute (route tokens by their top-k ids; row_offsets,
  * expert_ids, src_info; max_token_per_rank; fused_shared_expert) and fused_a2a,
- * HybridEPDispatch.forward (topk_idx [tokens, top_k] with -1 for unused slots; dispatched rows
- * grouped by expert).
+ * HybridEPDispatch.forward (compact per-token expert indices, a slot holding -1 carries no
+ * token; the dispatched rows come out grouped by expert).
  *
  *   topk_ids  [T*K] int32 device: expert id of each (token, slot) in [-1, E); -1 = unused.
  *   n_parts   P logical expert partitions: partition p owns experts [p*E/P, (p+1)*E/P).
@@ -127,10 +127,10 @@ int ep_dispatch_layout(const int32_t *topk_ids, int T, int K, int n_experts, int
 
 /*
  * ep_dispatch_nvfp4 -- scatter every token into its rows as NVFP4.
- * Defined by: Mojo EP dispatch, execute (each token is quantised to NVFP4 against its own
- * global scale 2688 / rowmax and sent to its experts; the receiver keeps the BF16 inverse of
- * that scale per row in output_rowwise_scales; output_scales holds the block scales;
- * scales_offsets the offsets into the scales buffer).
+ * Defined by: Mojo EP dispatch, execute (a token is sent to its experts as NVFP4, scaled by a
+ * per-token factor 2688 divided by the token's largest magnitude; the side that receives it
+ * stores that factor's reciprocal as BF16 per row in output_rowwise_scales; output_scales
+ * holds the per-block scales and scales_offsets tells where each group's scales begin).
  *
  *   input_tokens           [T*H] bf16.
  *   out_fp4                [R_max * H/2] uint8: E2M1 codes, element 2j in the low nibble of
@@ -159,10 +159,10 @@ int ep_dispatch_bf16(const uint16_t *input_tokens, int hidden_size, const ep_lay
 
 /*
  * ep_combine -- probability-weighted gather-reduce of the expert outputs into token order.
- * Defined by: fused_a2a, hybrid_ep_combine / HybridEPCombine.forward (expert outputs
- * [dispatched_tokens, hidden] -> combined hidden states in the original token order
- * [tokens, hidden]); token_dispatcher, TokenDispatcherConfig.moe_router_dtype (fp32 router
- * probabilities weight the expert outputs).
+ * Defined by: fused_a2a, hybrid_ep_combine / HybridEPCombine.forward (the expert outputs,
+ * one row per dispatched token, are brought back to one row per input token, in input order);
+ * token_dispatcher, TokenDispatcherConfig.moe_router_dtype (the router's fp32 probabilities
+ * are the weights).
  *   expert_out [R_max*H] bf16, probs [T*K] fp32  ->  out [T*H] bf16:
  *   out[t] = bf16( sum over k ascending with row_of[t,k] >= 0 of probs[t,k] * expert_out[row]
  *                  + (S ? expert_out[row_offsets[E] + t] : 0) ), accumulated in fp32.

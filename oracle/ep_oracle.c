@@ -123,8 +123,8 @@ float oracle_e4m3_decode(uint8_t code)
 
 /* ------------------------------------------------------------------------------------------
  * Layout [Mojo EP dispatch, execute: row_offsets, expert_ids, src_info;
- * fused_a2a, HybridEPDispatch.forward: output grouped by local expert, topk_idx with -1 for
- * unused slots; token_dispatcher, _assert_no_hybridep_overflow].
+ * fused_a2a, HybridEPDispatch.forward: the rows come out grouped by expert, and an index of
+ * -1 routes nowhere; token_dispatcher, _assert_no_hybridep_overflow].
  *
  * 1. An id outside [-1, E) sets BAD_EXPERT and is then treated as an unused slot.
  * 2. counts[e] = #{(t,k): id = e}; with a fused shared expert, group E holds one row per token.
@@ -343,7 +343,7 @@ void oracle_dispatch_bf16(const uint16_t *x, int T, int H, int K, int E, int S,
     }
 }
 
-/* Combine [fused_a2a, hybrid_ep_combine: expert outputs back in the original token order,
+/* Combine [fused_a2a, hybrid_ep_combine: expert outputs brought back to one row per input token,
  * shape [tokens, hidden]; token_dispatcher, TokenDispatcherConfig.moe_router_dtype: the
  * probabilities weight the expert outputs] and, with probs == NULL, the dispatch backward
  * pass [fused_a2a, HybridEPDispatch.backward: the dispatched rows' gradients are combined

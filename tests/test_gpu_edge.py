@@ -115,6 +115,17 @@ def test_ragged_last_tile_of_one_token(ep):
     full_check(ep, ids, x, p, y, 64, P=8)
 
 
+def test_layout_beyond_one_cluster(ep):
+    """T*K above what one thread-block cluster holds: the two-kernel layout (tile histograms,
+    scan by the last CTA, ranks) runs instead of the single-cluster one."""
+    ids, x, p, y = rand_case(17000, 8, 64, 16, 15, unused=0.03)
+    ids[5, 3] = 64                     # one bad id: flagged, then nothing written
+    ref = full_check(ep, ids, x, p, y, 64, P=4, S=1)
+    assert ref.status == oracle.BAD_EXPERT
+    ids[5, 3] = 7
+    full_check(ep, ids, x, p, y, 64, P=4, C=15000, S=1)
+
+
 def test_bad_expert_ids_write_nothing(ep):
     ids, x, p, y = rand_case(200, 4, 16, 64, 11)
     ids[17, 2] = 16
