@@ -53,12 +53,17 @@ def workload_config(cfg: W.Config) -> dict:
 
 def algorithmic_bytes(cfg: W.Config, R: int) -> dict:
     """Minimum bytes each kernel must move: x read once, every copy written once, every expert
-    row read once, the metadata once."""
-    T, H, K = cfg.T, cfg.H, cfg.K
+    row read once, the metadata once.  R = rows in use; R - S*T of them are routed rows."""
+    T, H, K, S = cfg.T, cfg.H, cfg.K, cfg.S
+    routed = R - S * T
     return {
         "layout": 4 * T * K + 12 * R + 4 * T * K,
         "dispatch_nvfp4": 2 * T * H + R * (H // 2 + H // 16 + 2),
         "combine": 2 * R * H + 8 * T * K + 2 * T * H,
+        # the rows the benchmark step does not run, timed on the same workload
+        "dispatch_bf16": 2 * T * H + 2 * R * H + 4 * T * K,
+        "combine_bwd": 2 * T * H + 2 * routed * H + 2 * R * H + 12 * T * K,
+        "dispatch_bwd": 2 * R * H + 4 * T * K + 2 * T * H,
     }
 
 
@@ -343,6 +348,33 @@ def run_ours(args, cfg):
     brk = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])]
                     for e in evb]).mean(axis=0) * 1e-3
 
+    # the other kernels of the path (BF16 dispatch and both backward passes), timed the same way
+    # on the same layout: events around each launch, L2 flushed before each
+    rows_bf16 = torch.empty(R_max, H, dtype=torch.bfloat16, device=dev)
+    g_out = torch.from_numpy(W.make_grad_out(cfg).view(np.int16)).to(dev).view(torch.bfloat16)
+    g_rows = torch.empty(R_max, H, dtype=torch.bfloat16, device=dev)
+    g_probs = torch.empty(T, K, dtype=torch.float32, device=dev)
+    g_x = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    extra_fns = {
+        "dispatch_bf16": lambda: ep.dispatch_bf16(x, L, out=rows_bf16, stream=stream),
+        "combine_bwd": lambda: ep.combine_bwd(g_out, y, probs, L, out=(g_rows, g_probs), stream=stream),
+        "dispatch_bwd": lambda: ep.dispatch_bwd(y, L, out=g_x, stream=stream),
+    }
+    extra = {}
+    for name, fn in extra_fns.items():
+        for _ in range(3):
+            flush_l2()
+            fn()
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(nb // 2)]
+        for a, b in pairs:
+            flush_l2()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        extra[name] = float(np.mean([a.elapsed_time(b) for a, b in pairs])) * 1e-3
+
     # ---- e2e through the public API with pinned host buffers ----
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
     hx = torch.from_numpy(inp["x"].view(np.int16)).pin_memory()
@@ -396,11 +428,13 @@ def run_ours(args, cfg):
     achieved = ab["combine"] / comb_s / 1e9
     traffic = recorded_traffic("combine")
     kernels = {}
-    for j, name in enumerate(("layout", "dispatch_nvfp4", "combine")):
-        gbs = ab[name] / brk[j] / 1e9
-        kernels[name] = {"us": brk[j] * 1e6, "algorithmic_bytes": ab[name], "GB/s": gbs,
+    times = dict(zip(("layout", "dispatch_nvfp4", "combine"), brk))
+    times.update(extra)
+    for name, sec in times.items():
+        gbs = ab[name] / sec / 1e9
+        kernels[name] = {"us": sec * 1e6, "algorithmic_bytes": ab[name], "GB/s": gbs,
                          "frac_of_measured_peak": gbs / peak}
-    step_bytes = sum(ab.values())
+    step_bytes = ab["layout"] + ab["dispatch_nvfp4"] + ab["combine"]
     step_s = total / args.steps
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -415,7 +449,9 @@ def run_ours(args, cfg):
                           "frac_of_measured_peak": step_bytes / step_s / 1e9 / peak,
                           "frac_of_8TB/s": step_bytes / step_s / 8e12},
         "kernels": kernels,
-        "kernels_note": f"mean of {nb} diagnostic steps after the timed region, events between kernels",
+        "kernels_note": (f"mean of {nb} diagnostic steps after the timed region, events between kernels; "
+                         "dispatch_bf16, combine_bwd and dispatch_bwd (not in the step) timed alone on "
+                         "the same layout, L2 flushed before each launch"),
         "e2e": {"value": ws * T * e2e_steps / e2e_t, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "path": "pinned host x/ids/probs/expert outputs -> device, layout + NVFP4 dispatch + "
