@@ -6,7 +6,8 @@ runs in the library's CUDA kernels.  There is no CPU fallback: importing the bin
 the built library raises.
 
 Entry points (same names as the C ABI, without the ``ep_`` prefix):
-``dispatch_layout``, ``dispatch_nvfp4``, ``dispatch_bf16``, ``combine``, ``combine_bwd``,
+``dispatch_layout``, ``dispatch_nvfp4``, ``dispatch_layout_nvfp4``, ``dispatch_bf16``, ``combine``,
+``combine_bwd``,
 ``dispatch_bwd``, ``read_status``, ``cvt_e2m1``, ``cvt_e4m3``.
 """
 from __future__ import annotations
@@ -64,6 +65,7 @@ SIGNATURES = {
     "ep_dispatch_layout": (_I, [_P, _I, _I, _I, _I, _I, _I, _LP, _P]),
     "ep_dispatch_layout_noalloc": (_I, [_P, _I, _I, _I, _I, _I, _I, _LP, _P]),
     "ep_dispatch_nvfp4": (_I, [_P, _I, _LP, _P, _P, _P, _P, _P]),
+    "ep_dispatch_layout_nvfp4": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _I, _LP, _P, _P, _P, _P, _P]),
     "ep_dispatch_bf16": (_I, [_P, _I, _LP, _P, _P]),
     "ep_combine": (_I, [_P, _P, _I, _LP, _P, _P]),
     "ep_combine_bwd": (_I, [_P, _P, _P, _I, _LP, _P, _P, _P]),
@@ -254,6 +256,45 @@ def dispatch_nvfp4(x: torch.Tensor, L: Layout, out=None, stream=None):
                                 _stream(stream))
     _check(rc, "ep_dispatch_nvfp4")
     return out
+
+
+def dispatch_layout_nvfp4(topk_ids: torch.Tensor, x: torch.Tensor, n_experts: int, n_parts: int = 1,
+                          capacity: int | None = None, fused_shared: bool = False,
+                          out_layout: Layout | None = None, out=None, stream=None):
+    """ep_dispatch_layout_nvfp4: layout + NVFP4 dispatch in one call (the quantisation overlaps
+    the layout).  Returns (Layout, (fp4, scales, inv, scales_offsets))."""
+    if topk_ids.dtype != torch.int32 or topk_ids.dim() != 2:
+        raise TypeError("topk_ids must be an int32 [T, K] tensor")
+    T, K = topk_ids.shape
+    Tx, H = x.shape
+    if Tx != T:
+        raise ValueError("x and topk_ids disagree on the number of tokens")
+    S = int(bool(fused_shared))
+    L = out_layout
+    if L is not None and (L.T, L.K, L.E, L.P, L.S) != (T, K, n_experts, n_parts, S):
+        raise ValueError("layout buffers were allocated for other sizes "
+                         f"{(L.T, L.K, L.E, L.P, L.S)}")
+    if L is None:
+        L = Layout(T, K, n_experts, n_parts, fused_shared, topk_ids.device)
+    _need(x, None, H, _BF16, "input_tokens", exact_rows=T)
+    if out is None:
+        dev = x.device
+        out = (torch.empty(max(L.R_max, 1), H // 2, dtype=torch.uint8, device=dev),
+               torch.empty(max(L.R_max, 1), H // 16, dtype=torch.uint8, device=dev),
+               torch.empty(max(L.R_max, 1), dtype=torch.bfloat16, device=dev),
+               torch.empty(L.G + 1, dtype=torch.int32, device=dev))
+    fp4, sc, inv, so = out
+    _need(fp4, L.R_max, H // 2, (torch.uint8,), "out_fp4")
+    _need(sc, L.R_max, H // 16, (torch.uint8,), "out_scales")
+    _need(inv, L.R_max, None, _BF16, "out_rowwise_inv_scale")
+    _need(so, L.G + 1, None, (torch.int32,), "scales_offsets")
+    cap = T if capacity is None else int(capacity)
+    L.capacity = cap
+    rc = _lib.ep_dispatch_layout_nvfp4(_ptr(topk_ids) if T > 0 else None, T, K, n_experts, n_parts, cap,
+                                       S, _bits(x) if T > 0 else None, H, L.ref, _ptr(fp4), _ptr(sc),
+                                       _bits(inv), _ptr(so), _stream(stream))
+    _check(rc, "ep_dispatch_layout_nvfp4")
+    return L, out
 
 
 def dispatch_bf16(x: torch.Tensor, L: Layout, out: torch.Tensor | None = None, stream=None):

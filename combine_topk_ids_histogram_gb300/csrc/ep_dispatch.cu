@@ -50,19 +50,23 @@ __device__ __forceinline__ float absmax8(uint4 v) {
 template <int BPT, int MAXT, int MINB>
 __global__ void __launch_bounds__(MAXT, MINB)
 ep_dispatch_nvfp4_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int E, int S, int G, int R_max,
+                         int early,
                          const int32_t *__restrict__ row_of, const int32_t *__restrict__ row_offsets,
                          const int32_t *__restrict__ status, uint8_t *__restrict__ out_fp4,
                          uint8_t *__restrict__ out_scales, uint16_t *__restrict__ out_inv,
                          int32_t *__restrict__ scales_offsets) {
     __shared__ int s_rows[kMaxRowsPerToken];
     __shared__ float s_red[32];
-    pdl_begin();
+    // early == 0: wait for the previous kernel first; the token row, the row indices and the
+    //             status word are then all requested before any is used.
+    // early == 1: the kernel directly follows the layout of the same call (which let it launch
+    //             only once every earlier kernel had completed), so x is read and quantised
+    //             while the layout still runs, and the layout's outputs are read after the wait.
+    if (!early) pdl_begin();
     const int tid = threadIdx.x;
     const int t = blockIdx.x;
     const int nth = H / (16 * BPT);
     const bool active = tid < nth && t < T;
-    // The token row, the row indices and the status word are all requested before any of them
-    // is used, so a CTA waits for memory once.
     uint4 v[2 * BPT];
     if (active) {
         const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H) + (size_t)tid * 2 * BPT;
@@ -73,16 +77,10 @@ ep_dispatch_nvfp4_kernel(const uint16_t *__restrict__ x, int T, int H, int K, in
         for (int i = 0; i < 2 * BPT; ++i) v[i] = make_uint4(0, 0, 0, 0);
     }
     int my_row = -1;
-    if (t < T) {
+    if (!early && t < T) {
         if (tid < K) my_row = row_of[(size_t)t * K + tid];
         else if (tid == K && S) my_row = row_offsets[E] + t;
     }
-    if (load_status(status)) return;
-    if (t == 0)
-        for (int g = tid; g <= G; g += blockDim.x) scales_offsets[g] = row_offsets[g];
-    if (t >= T) return;
-    const int nrows = K + S;
-    if (tid < nrows) s_rows[tid] = my_row;
     float bmax[BPT];
     float tmax = 0.0f;
 #pragma unroll
@@ -97,6 +95,20 @@ ep_dispatch_nvfp4_kernel(const uint16_t *__restrict__ x, int T, int H, int K, in
         g = __fdiv_rn(2688.0f, a);
         if (isinf(g)) g = FLT_MAX;
     }
+    if (early) {
+        pdl_begin();
+        if (t < T) {
+            if (tid < K) my_row = row_of[(size_t)t * K + tid];
+            else if (tid == K && S) my_row = row_offsets[E] + t;
+        }
+    }
+    if (load_status(status)) return;
+    if (t == 0)
+        for (int gi = tid; gi <= G; gi += blockDim.x) scales_offsets[gi] = row_offsets[gi];
+    if (t >= T) return;
+    const int nrows = K + S;
+    if (tid < nrows) s_rows[tid] = my_row;
+    __syncthreads();
     if (!active) return;
 
     uint32_t codes[2 * BPT];
@@ -176,10 +188,12 @@ inline int launch_cvt(const float *in, uint8_t *codes, long n, void *stream, int
 
 using namespace ep;
 
-extern "C" int ep_dispatch_nvfp4(const uint16_t *input_tokens, int hidden_size, const ep_layout_t *L,
-                                 uint8_t *out_fp4, uint8_t *out_scales, uint16_t *out_rowwise_inv_scale,
-                                 int32_t *scales_offsets, void *stream) {
-    const int H = hidden_size;
+namespace ep {
+namespace {
+
+int launch_nvfp4(const uint16_t *input_tokens, int H, const ep_layout_t *L, uint8_t *out_fp4,
+                 uint8_t *out_scales, uint16_t *out_rowwise_inv_scale, int32_t *scales_offsets,
+                 int early, cudaStream_t st) {
     if (!layout_ok(L) || !hidden_ok(H)) return EP_ERR_INVALID_ARG;
     const int bpt = (H % 32 == 0) ? 2 : 1;
     const int nth = H / (16 * bpt);
@@ -195,11 +209,10 @@ extern "C" int ep_dispatch_nvfp4(const uint16_t *input_tokens, int hidden_size, 
     const int grid = L->T > 0 ? L->T : 1;
     const int G = L->E + L->fused_shared;
     const int R_max = (int)rows_max(L->T, L->K, L->fused_shared);
-    cudaStream_t st = as_stream(stream);
     const int32_t *row_of = L->row_of, *row_offsets = L->row_offsets, *status = L->status;
 #define EP_NVFP4_LAUNCH(BPT, MAXT, MINB)                                                        \
     return launch_pdl(ep_dispatch_nvfp4_kernel<BPT, MAXT, MINB>, dim3(grid), dim3(threads), 0, st, \
-                      input_tokens, L->T, H, L->K, L->E, L->fused_shared, G, R_max, row_of,     \
+                      input_tokens, L->T, H, L->K, L->E, L->fused_shared, G, R_max, early, row_of, \
                       row_offsets, status, out_fp4, out_scales, out_rowwise_inv_scale,          \
                       scales_offsets)
     // Up to 256 threads (H <= 8192): 5 such CTAs per SM without spilling.
@@ -208,6 +221,40 @@ extern "C" int ep_dispatch_nvfp4(const uint16_t *input_tokens, int hidden_size, 
     if (threads <= 256) EP_NVFP4_LAUNCH(1, 256, 5);
     EP_NVFP4_LAUNCH(1, 1024, 1);
 #undef EP_NVFP4_LAUNCH
+}
+
+}  // namespace
+}  // namespace ep
+
+extern "C" int ep_dispatch_nvfp4(const uint16_t *input_tokens, int hidden_size, const ep_layout_t *L,
+                                 uint8_t *out_fp4, uint8_t *out_scales, uint16_t *out_rowwise_inv_scale,
+                                 int32_t *scales_offsets, void *stream) {
+    return launch_nvfp4(input_tokens, hidden_size, L, out_fp4, out_scales, out_rowwise_inv_scale,
+                        scales_offsets, 0, as_stream(stream));
+}
+
+extern "C" int ep_dispatch_layout_nvfp4(const int32_t *topk_ids, int T, int K, int n_experts,
+                                        int n_parts, int capacity, int fused_shared,
+                                        const uint16_t *input_tokens, int hidden_size,
+                                        ep_layout_t *L, uint8_t *out_fp4, uint8_t *out_scales,
+                                        uint16_t *out_rowwise_inv_scale, int32_t *scales_offsets,
+                                        void *stream) {
+    const int H = hidden_size;
+    if (!hidden_ok(H) || H / 16 > 1024) return EP_ERR_INVALID_ARG;
+    if ((T > 0 && (!input_tokens || !out_fp4 || !out_scales || !out_rowwise_inv_scale)) ||
+        !scales_offsets)
+        return EP_ERR_INVALID_ARG;
+    const void *ptrs[] = {input_tokens, out_fp4, out_scales, out_rowwise_inv_scale, scales_offsets};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return EP_ERR_INVALID_ARG;
+    cudaStream_t st = as_stream(stream);
+    int rc = launch_layout(topk_ids, T, K, n_experts, n_parts, capacity, fused_shared, L, st, nullptr);
+    if (rc != EP_OK) return rc;
+    // The dispatch kernel directly follows the layout kernel, which lets it launch only once
+    // every earlier kernel of the stream has completed, so its CTAs read and quantise their
+    // tokens while the layout is still running and wait for the layout only before storing.
+    return launch_nvfp4(input_tokens, H, L, out_fp4, out_scales, out_rowwise_inv_scale,
+                        scales_offsets, 1, st);
 }
 
 extern "C" int ep_dispatch_bf16(const uint16_t *input_tokens, int hidden_size, const ep_layout_t *L,

@@ -89,4 +89,9 @@ inline int resident_blocks(K kernel, int threads, size_t smem) {
     return blocks;
 }
 
+// Enqueues a dispatch layout (ep_layout.cu).  *cluster_ctas_used receives the number of SMs the
+// single-cluster layout kernel occupies, or 0 when the two-kernel path ran.
+int launch_layout(const int32_t *topk_ids, int T, int K, int E, int P, int capacity, int S,
+                  ep_layout_t *L, cudaStream_t st, int *cluster_ctas_used);
+
 }  // namespace ep

@@ -740,9 +740,10 @@ inline int max_cluster_ctas() {
 // The whole layout as one cluster of CTAs (see ep_layout_cluster_kernel).  Returns -1 when the
 // sizes do not fit one cluster (the caller then uses the two-kernel path).
 inline int launch_cluster_layout(const int32_t *ids, int T, int K, int E, int P, int C, int S,
-                                 ep_layout_t *L, cudaStream_t st) {
+                                 ep_layout_t *L, cudaStream_t st, int *ctas_used) {
     const int ncta = cluster_ctas(T, K, E, P, max_cluster_ctas());
     if (ncta == 0) return -1;
+    *ctas_used = ncta;
     const int tile_t = (T + ncta - 1) / ncta;
     const size_t smem = cluster_smem_bytes(E, P, tile_t, K);
     if (cudaFuncSetAttribute(ep_layout_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -781,10 +782,13 @@ extern "C" size_t ep_layout_workspace_bytes(int T, int K, int n_experts, int fus
     return workspace_bytes(num_tiles(T, tt), n_experts);
 }
 
-extern "C" int ep_dispatch_layout(const int32_t *topk_ids, int T, int K, int n_experts,
-                                  int n_parts, int capacity, int fused_shared, ep_layout_t *L,
-                                  void *stream) {
-    const int E = n_experts, P = n_parts, S = fused_shared;
+namespace ep {
+
+// Validates the arguments of a layout call and enqueues it.  *cluster_ctas_used receives the
+// number of SMs the single-cluster kernel occupies (0 when the two-kernel path ran).
+int launch_layout(const int32_t *topk_ids, int T, int K, int E, int P, int capacity, int S,
+                  ep_layout_t *L, cudaStream_t st, int *cluster_ctas_used) {
+    if (cluster_ctas_used) *cluster_ctas_used = 0;
     if (!L || !sizes_ok(T, K, E, S)) return EP_ERR_INVALID_ARG;
     if (P < 1 || P > E || E % P != 0 || capacity < 0) return EP_ERR_INVALID_ARG;
     if ((T > 0 && !topk_ids) || !L->row_offsets || !L->expert_ids || !L->src_info ||
@@ -805,15 +809,17 @@ extern "C" int ep_dispatch_layout(const int32_t *topk_ids, int T, int K, int n_e
     L->capacity = capacity;
     L->fused_shared = S;
 
-    cudaStream_t st = as_stream(stream);
-    const int rc_cl = launch_cluster_layout(topk_ids, T, K, E, P, capacity, S, L, st);
-    if (rc_cl != -1) return rc_cl;
+    int used = 0;
+    const int rc_cl = launch_cluster_layout(topk_ids, T, K, E, P, capacity, S, L, st, &used);
+    if (rc_cl != -1) {
+        if (cluster_ctas_used) *cluster_ctas_used = used;
+        return rc_cl;
+    }
     Workspace ws = carve(L->workspace, nTiles, E);
     const size_t smem_count = count_smem_bytes(E, P, tt, K);
     int rc = launch_pdl(ep_layout_count_kernel, dim3(nTiles), dim3(kLayoutThreads), smem_count, st,
                         topk_ids, T, K, E, P, capacity, S, tt, nTiles, magic_of(E / P), ws,
-                        L->row_offsets,
-                        L->part_tokens, L->status);
+                        L->row_offsets, L->part_tokens, L->status);
     if (rc != EP_OK) return rc;
     size_t smem_rank = sizeof(int) * ((size_t)kLayoutWarps * E + (size_t)tt * K);
     if (smem_rank > 48 * 1024 &&
@@ -823,6 +829,15 @@ extern "C" int ep_dispatch_layout(const int32_t *topk_ids, int T, int K, int n_e
     return launch_pdl(ep_layout_rank_kernel, dim3(nTiles), dim3(kLayoutThreads), smem_rank, st,
                       topk_ids, T, K, E, S, tt, nTiles, key_bits(E + 1), (const int32_t *)ws.cnt,
                       (const int32_t *)L->row_offsets, L->row_of, L->src_info, L->expert_ids);
+}
+
+}  // namespace ep
+
+extern "C" int ep_dispatch_layout(const int32_t *topk_ids, int T, int K, int n_experts,
+                                  int n_parts, int capacity, int fused_shared, ep_layout_t *L,
+                                  void *stream) {
+    return launch_layout(topk_ids, T, K, n_experts, n_parts, capacity, fused_shared, L,
+                         as_stream(stream), nullptr);
 }
 
 extern "C" int ep_read_status(const ep_layout_t *L, void *stream, int32_t *host_status) {

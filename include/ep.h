@@ -149,6 +149,26 @@ int ep_dispatch_nvfp4(const uint16_t *input_tokens, int hidden_size, const ep_la
                       int32_t *scales_offsets, void *stream);
 
 /*
+ * ep_dispatch_layout_nvfp4 -- ep_dispatch_layout followed by ep_dispatch_nvfp4, in one call.
+ * Defined by: fused_a2a, HybridEPDispatch.forward (routing metadata and the permuted copy of
+ * the tokens produced by one dispatch; fuse_permute) and Mojo EP dispatch, execute (routing by
+ * top-k ids and NVFP4 quantisation in one operation).
+ *
+ * Arguments are those of ep_dispatch_layout followed by those of ep_dispatch_nvfp4, and the
+ * results are identical to calling the two in sequence.  Doing both in one call lets the
+ * quantisation of input_tokens overlap the layout computation: the dispatch kernel launches
+ * on the SMs the layout leaves free and its CTAs read and quantise their tokens before the
+ * layout has finished (safe because input_tokens, like every argument, must be complete in
+ * stream order when the call is made); they wait for the layout only before storing.  Errors
+ * are those of the two calls.
+ */
+int ep_dispatch_layout_nvfp4(const int32_t *topk_ids, int T, int K, int n_experts, int n_parts,
+                             int capacity, int fused_shared, const uint16_t *input_tokens,
+                             int hidden_size, ep_layout_t *L, uint8_t *out_fp4,
+                             uint8_t *out_scales, uint16_t *out_rowwise_inv_scale,
+                             int32_t *scales_offsets, void *stream);
+
+/*
  * ep_dispatch_bf16 -- scatter every token into its rows unchanged.
  * Defined by: fused_a2a, HybridEPDispatch.forward / hybrid_ep_dispatch (dispatched hidden
  * states [dispatched_tokens, hidden] grouped by expert).

@@ -130,3 +130,39 @@ def test_layout_reuse_across_calls(ep):
         L.src_info.fill_(-7)
         ep.dispatch_layout(dev(ids), E, P, C, True, out=L)
         check_layout(L, oracle.layout(ids, E, P=P, C=C, S=S), ep)
+
+
+FUSED_CASES = [("tiny", None, None), ("dsv3", 900, None), ("qwen3", 1500, None),
+               ("dsv3", 7000, 7000),            # more tokens per CTA than staging slots: rounds
+               ("dsv3_large", 1000, 610)]       # capacity overflow: nothing written
+
+
+@pytest.mark.parametrize("name,T,C", FUSED_CASES, ids=[f"{c[0]}-{c[1]}" for c in FUSED_CASES])
+def test_fused_layout_nvfp4(ep, name, T, C):
+    """ep_dispatch_layout_nvfp4 gives exactly the layout and NVFP4 rows of the two calls."""
+    cfg = W.CONFIGS[name]
+    kw = {"C": C} if C is not None else {}
+    cfg = W.scaled(cfg, T=T, **kw) if (T or kw) else cfg
+    inp = W.make_inputs(cfg)
+    x, ids = inp["x"], inp["topk_ids"]
+    E, K, S, P, Cap, H = cfg.E, cfg.K, cfg.S, cfg.P, cfg.capacity, cfg.H
+    ref = oracle.layout(ids, E, P=P, C=Cap, S=S)
+    L = new_layout(ep, cfg.T, K, E, P, S)
+    R_max = ref.R_max
+    out = (torch.full((R_max, H // 2), 0xA5, dtype=torch.uint8, device="cuda"),
+           torch.full((R_max, H // 16), 0xA5, dtype=torch.uint8, device="cuda"),
+           torch.full((R_max,), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16),
+           torch.full((E + S + 1,), -7, dtype=torch.int32, device="cuda"))
+    for _ in range(2):   # twice in a row on the same buffers
+        ep.dispatch_layout_nvfp4(dev(ids), dev_bf16(x), E, P, Cap, bool(S), out_layout=L, out=out)
+        check_layout(L, ref, ep)
+        rfp4, rsc, rinv, rso = oracle.dispatch_nvfp4(x, ref, fill=0xA5)
+        fp4, sc, inv, so = out
+        if ref.status:
+            assert (fp4 == 0xA5).all() and (sc == 0xA5).all() and (so == -7).all()
+            assert (inv.view(torch.int16) == -1).all()
+        else:
+            assert np.array_equal(fp4.cpu().numpy(), rfp4)
+            assert np.array_equal(sc.cpu().numpy(), rsc)
+            assert np.array_equal(host_bf16(inv)[:ref.R], rinv[:ref.R])
+            assert np.array_equal(so.cpu().numpy(), rso)
