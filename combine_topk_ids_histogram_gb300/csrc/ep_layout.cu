@@ -73,12 +73,17 @@ __device__ __forceinline__ bool bad_id(int id, int E) { return id < -1 || id >= 
 
 // Lanes of the warp whose key equals this lane's (keys in [0, 2^nbits)): the intersection, over
 // the key's bits, of the lanes that agree with this lane on that bit -- one ballot per bit.
+constexpr int kMaxKeyBits = 11;   // keys id + 1 in [0, kMaxE]
+
 __device__ __forceinline__ unsigned same_key_lanes(unsigned key, int nbits) {
     unsigned peers = kFullMask;
-    for (int b = 0; b < nbits; ++b) {
-        const unsigned bit = (key >> b) & 1u;
-        const unsigned m = __ballot_sync(kFullMask, bit);
-        peers &= bit ? m : ~m;
+#pragma unroll
+    for (int b = 0; b < kMaxKeyBits; ++b) {   // unrolled: the ballots are independent
+        if (b < nbits) {
+            const unsigned bit = (key >> b) & 1u;
+            const unsigned m = __ballot_sync(kFullMask, bit);
+            peers &= bit ? m : ~m;
+        }
     }
     return peers;
 }
@@ -419,6 +424,7 @@ ep_layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int 
 // ---------------------------------------------------------------------------------------
 constexpr int kClThreads = 1024;
 constexpr int kClWarps = kClThreads / 32;
+static_assert(kClWarps == 32, "the cluster kernel scans per-warp values with one warp");
 constexpr int kClMaxCtas = 16;            // largest cluster (non-portable; 8 where 16 is refused)
 constexpr int kClMaxIds = 8192;           // ids of one CTA's range held in shared memory
 constexpr int kClIdsPerCta = 2048;        // below this many ids per CTA, use fewer CTAs
@@ -489,6 +495,7 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
     __shared__ int s_warp[kClWarps];
     __shared__ int s_warp2[kClWarps];
     __shared__ int s_bad;
+    __shared__ int s_routed, s_nvalid;
 
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
@@ -544,16 +551,30 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
 
     // B. per-(warp, expert) exclusive prefix over the warps, and the CTA's count per expert:
     //    warp w scans experts w, w + 32, ...; lane l holds warp l's count.
-    for (int e = warp; e < E; e += kClWarps) {
-        const int c = s_whist[lane * EP + e];
-        int incl = c;
+    for (int e0 = warp; e0 < E; e0 += 4 * kClWarps) {   // four independent scans interleaved
+        int c[4], incl[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int e = e0 + q * kClWarps;
+            c[q] = e < E ? s_whist[lane * EP + e] : 0;
+            incl[q] = c[q];
+        }
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(kFullMask, incl, o);
-            if (lane >= o) incl += v;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int v = __shfl_up_sync(kFullMask, incl[q], o);
+                if (lane >= o) incl[q] += v;
+            }
         }
-        s_whist[lane * EP + e] = incl - c;
-        if (lane == 31) s_hist[e] = incl;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int e = e0 + q * kClWarps;
+            if (e < E) {
+                s_whist[lane * EP + e] = incl[q] - c[q];
+                if (lane == 31) s_hist[e] = incl[q];
+            }
+        }
     }
     //    tokens per partition: warp w counts partitions w, w + 32, ... from the token masks
     if (masks) {
@@ -602,6 +623,21 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
         }
         mine += total[q];
     }
+    //    CTA 0: partition totals against the capacity, and the bad-id flags (status bits kept
+    //    above bit 4 of s_bad, whose low bit is this CTA's own bad-id flag)
+    if (crank == 0) {
+        int f = 0;
+        for (int p = tid; p < P; p += kClThreads) {
+            int c = 0;
+            for (int r = 0; r < ncta; ++r) c += s_part_all[r * P + p];
+            part_tokens[p] = c;
+            if (c > C) f |= EP_STATUS_OVERFLOW;
+        }
+        if (tid < ncta && s_bad_all[tid]) f |= EP_STATUS_BAD_EXPERT;
+        if (f) atomicOr(&s_bad, f << 4);
+    }
+    //    exclusive scans over experts (thread-major) of the cluster totals and of this CTA's
+    //    counts: within each warp, then one warp over the warp sums
     int incl = mine, incl_l = mine_local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -616,32 +652,31 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
         s_warp[warp] = incl;
         s_warp2[warp] = incl_l;
     }
-    int over = 0, any_bad = 0;
-    if (crank == 0) {
-        for (int p = tid; p < P; p += kClThreads) {
-            int c = 0;
-            for (int r = 0; r < ncta; ++r) c += s_part_all[r * P + p];
-            part_tokens[p] = c;
-            if (c > C) over = 1;
+    __syncthreads();
+    if (warp == 0) {
+        const int va0 = s_warp[lane], vb0 = s_warp2[lane];
+        int ia = va0, ib = vb0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int va = __shfl_up_sync(kFullMask, ia, o);
+            const int vb = __shfl_up_sync(kFullMask, ib, o);
+            if (lane >= o) {
+                ia += va;
+                ib += vb;
+            }
         }
-        if (tid < ncta && s_bad_all[tid]) any_bad = 1;
-    }
-    // __syncthreads_or returns a predicate, so each status bit is reduced on its own; the
-    // barrier also publishes s_warp / s_warp2.
-    over = __syncthreads_or(over);
-    any_bad = __syncthreads_or(any_bad);
-    const int flags = (over ? EP_STATUS_OVERFLOW : 0) | (any_bad ? EP_STATUS_BAD_EXPERT : 0);
-    int routed = 0, warp_before = 0, warp_before_l = 0, n_valid = 0;
-    for (int w = 0; w < kClWarps; ++w) {
-        if (w < warp) {
-            warp_before += s_warp[w];
-            warp_before_l += s_warp2[w];
+        s_warp[lane] = ia - va0;   // exclusive warp offsets
+        s_warp2[lane] = ib - vb0;
+        if (lane == 31) {
+            s_routed = ia;
+            s_nvalid = ib;
         }
-        routed += s_warp[w];
-        n_valid += s_warp2[w];
     }
-    int excl = warp_before + incl - mine;
-    int excl_l = warp_before_l + incl_l - mine_local;
+    __syncthreads();
+    const int routed = s_routed, n_valid = s_nvalid;
+    const int flags = crank == 0 ? (s_bad >> 4) : 0;
+    int excl = s_warp[warp] + incl - mine;
+    int excl_l = s_warp2[warp] + incl_l - mine_local;
 #pragma unroll
     for (int q = 0; q < kClExpertsPerThread; ++q) {
         const int e = kClExpertsPerThread * tid + q;
