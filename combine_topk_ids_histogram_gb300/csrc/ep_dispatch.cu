@@ -9,6 +9,7 @@
 // E4M3 and E2M1 encodings are single hardware conversions, and the same bytes are then
 // stored to each of the token's K (+1 shared) rows.
 #include "ep_common.cuh"
+#include "ep_async.cuh"
 #include "ep_host.h"
 
 namespace ep {
@@ -167,6 +168,156 @@ ep_dispatch_bf16_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// Staged NVFP4 dispatch (H % 256 == 0, H <= 8192): as many CTAs as fit on the GPU (several per
+// SM), each owning a contiguous range of tokens, with the per-token kernel's thread layout (one
+// thread per 32 elements).  In rounds of up to kStageSlots tokens:
+//   phase 1: quantise the round's tokens into shared memory (codes, block scales, inverse
+//            scale per staging slot), the next token's row already loading into registers;
+//   phase 2: copy every staged row to each of its K (+1) destination rows with bulk
+//            asynchronous copies (shared -> global).
+// With `early` set the kernel directly follows the layout kernel of the same call (which let it
+// launch only once every earlier kernel had completed), so phase 1 of the first round runs
+// before waiting for the layout and overlaps it; the layout's outputs are read after the wait.
+// ---------------------------------------------------------------------------------------
+constexpr int kStageSlots = 8;
+constexpr int kStageMaxThreads = 256;
+
+__global__ void __launch_bounds__(kStageMaxThreads, 4)
+ep_dispatch_nvfp4_staged_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int E, int S, int G,
+                                int R_max, int tpc, int early, const int32_t *__restrict__ row_of,
+                                const int32_t *__restrict__ row_offsets,
+                                const int32_t *__restrict__ status, uint8_t *__restrict__ out_fp4,
+                                uint8_t *__restrict__ out_scales, uint16_t *__restrict__ out_inv,
+                                int32_t *__restrict__ scales_offsets) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    __shared__ float s_red[2][kStageMaxThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int nth = H / 32;
+    const bool active = tid < nth;
+    const unsigned code_bytes = (unsigned)H / 2, scale_bytes = (unsigned)H / 16;
+    const unsigned slot_bytes = code_bytes + scale_bytes;   // a multiple of 16
+    unsigned char *s_stage = smem_raw;                    // [kStageSlots][slot_bytes]
+    uint16_t *s_inv = reinterpret_cast<uint16_t *>(smem_raw + (size_t)kStageSlots * slot_bytes);
+    const int tb = blockIdx.x * tpc, te = min(T, tb + tpc);
+    bool waited = false;
+    if (!early) {
+        pdl_begin();
+        waited = true;
+    }
+    const uint4 *xv = reinterpret_cast<const uint4 *>(x);
+    uint4 v[4], vn[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = vn[i] = make_uint4(0, 0, 0, 0);
+    if (active && tb < te) {
+        const uint4 *src = xv + ((size_t)tb * H) / 8 + 4 * tid;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = ld_stream(src + i);
+    }
+    for (int r0 = tb; r0 < te; r0 += kStageSlots) {
+        const int r1 = min(te, r0 + kStageSlots);
+        // ---- phase 1
+        for (int t = r0; t < r1; ++t) {
+            const int slot = t - r0, par = (t - tb) & 1;
+            if (active && t + 1 < te) {
+                const uint4 *src = xv + ((size_t)(t + 1) * H) / 8 + 4 * tid;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) vn[i] = ld_stream(src + i);
+            }
+            const float b0 = fmaxf(absmax8(v[0]), absmax8(v[1]));
+            const float b1 = fmaxf(absmax8(v[2]), absmax8(v[3]));
+            float m = fmaxf(b0, b1);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFullMask, m, o));
+            if (lane == 0) s_red[par][warp] = m;
+            __syncthreads();
+            float a = 0.0f;
+            for (int w = 0; w < nwarps; ++w) a = fmaxf(a, s_red[par][w]);
+            float g = 1.0f;
+            if (a != 0.0f) {
+                g = __fdiv_rn(2688.0f, a);
+                if (isinf(g)) g = FLT_MAX;
+            }
+            unsigned char *slotp = s_stage + (size_t)slot * slot_bytes;
+            if (active) {
+                uint32_t s0, s1;
+                const uint2 c0 = quant_block(v[0], v[1], b0, g, s0);
+                const uint2 c1 = quant_block(v[2], v[3], b1, g, s1);
+                *reinterpret_cast<uint4 *>(slotp + 16 * tid) = make_uint4(c0.x, c0.y, c1.x, c1.y);
+                *reinterpret_cast<unsigned short *>(slotp + code_bytes + 2 * tid) =
+                    (unsigned short)(s0 | (s1 << 8));
+            }
+            if (tid == 0) {
+                __nv_bfloat16 h = __float2bfloat16_rn(__frcp_rn(g));
+                s_inv[slot] = *reinterpret_cast<uint16_t *>(&h);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = vn[i];
+        }
+        fence_proxy_async_smem();   // the staged bytes become visible to the bulk-copy engine
+        __syncthreads();
+        if (!waited) {              // from here on the layout's outputs are needed
+            pdl_begin();
+            waited = true;
+        }
+        if (load_status(status)) return;   // constant per call: no copy was issued before
+        if (blockIdx.x == 0 && r0 == tb)
+            for (int gi = tid; gi <= G; gi += blockDim.x) scales_offsets[gi] = row_offsets[gi];
+        // ---- phase 2
+        const int shared_base = S ? row_offsets[E] : 0;
+        const int nrows = K + S;
+        for (int j = warp; j < r1 - r0; j += nwarps) {
+            const int t = r0 + j;
+            const unsigned char *slotp = s_stage + (size_t)j * slot_bytes;
+            for (int k = lane; k < nrows; k += 32) {
+                const int r = k < K ? row_of[(size_t)t * K + k] : shared_base + t;
+                if (r < 0 || r >= R_max) continue;
+                bulk_store(out_fp4 + (size_t)r * code_bytes, slotp, code_bytes);
+                bulk_store(out_scales + (size_t)r * scale_bytes, slotp + code_bytes, scale_bytes);
+                out_inv[r] = s_inv[j];
+            }
+        }
+        bulk_commit();
+        bulk_wait_read_all();       // the staging slots may be overwritten after this
+        __syncthreads();
+    }
+    if (!waited) pdl_begin();       // a CTA without tokens still orders itself after the layout
+    bulk_wait_all();                // every copy of this thread has landed
+}
+
+// Staged dispatch on as many CTAs as fit; -1 when the shape does not suit it.
+inline int launch_nvfp4_staged(const uint16_t *x, int H, const ep_layout_t *L, uint8_t *out_fp4,
+                               uint8_t *out_scales, uint16_t *out_inv, int32_t *scales_offsets,
+                               int early, int busy_sms, cudaStream_t st) {
+    const int T = L->T;
+    if (T == 0 || H % 256 != 0 || H / 32 > kStageMaxThreads) return -1;
+    const int threads = max(H / 32, 32 * ((L->K + 1 + 31) / 32));
+    if (threads > kStageMaxThreads) return -1;
+    const size_t smem = (size_t)kStageSlots * ((size_t)H / 2 + H / 16) + 2 * kStageSlots;
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(ep_dispatch_nvfp4_staged_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return -1;
+    }
+    int grid = resident_blocks(ep_dispatch_nvfp4_staged_kernel, threads, smem);
+    if (grid <= 0) return -1;
+    int dev = 0, sms = 0;
+    if (busy_sms > 0 && cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > busy_sms)
+        grid = grid / sms * (sms - busy_sms);   // only the SMs the layout leaves free
+    if (grid <= 0) return -1;
+    const int tpc = (T + grid - 1) / grid;
+    grid = (T + tpc - 1) / tpc;
+    const int G = L->E + L->fused_shared;
+    const int R_max = (int)rows_max(L->T, L->K, L->fused_shared);
+    return launch_pdl(ep_dispatch_nvfp4_staged_kernel, dim3(grid), dim3(threads), smem, st, x, T, H,
+                      L->K, L->E, L->fused_shared, G, R_max, tpc, early, (const int32_t *)L->row_of,
+                      (const int32_t *)L->row_offsets, (const int32_t *)L->status, out_fp4, out_scales,
+                      out_inv, scales_offsets);
+}
+
 __global__ void ep_cvt_kernel(const float *__restrict__ in, uint8_t *__restrict__ codes, long n, int e4m3) {
     for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
         const float v = in[i];
@@ -248,11 +399,15 @@ extern "C" int ep_dispatch_layout_nvfp4(const int32_t *topk_ids, int T, int K, i
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return EP_ERR_INVALID_ARG;
     cudaStream_t st = as_stream(stream);
-    int rc = launch_layout(topk_ids, T, K, n_experts, n_parts, capacity, fused_shared, L, st, nullptr);
+    int layout_sms = 0;
+    int rc = launch_layout(topk_ids, T, K, n_experts, n_parts, capacity, fused_shared, L, st, &layout_sms);
     if (rc != EP_OK) return rc;
     // The dispatch kernel directly follows the layout kernel, which lets it launch only once
     // every earlier kernel of the stream has completed, so its CTAs read and quantise their
     // tokens while the layout is still running and wait for the layout only before storing.
+    rc = launch_nvfp4_staged(input_tokens, H, L, out_fp4, out_scales, out_rowwise_inv_scale,
+                             scales_offsets, 1, layout_sms, st);
+    if (rc != -1) return rc;
     return launch_nvfp4(input_tokens, H, L, out_fp4, out_scales, out_rowwise_inv_scale,
                         scales_offsets, 1, st);
 }

@@ -5,6 +5,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <utility>
 
 #include "ep.h"
@@ -68,24 +69,35 @@ inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sm
 }
 
 // Blocks of `kernel` that fit on the device at once (SM count x resident blocks per SM),
-// for grids that loop over their work.  Cached per device.
+// for grids that loop over their work.  Cached per (device, kernel, block size, shared memory).
 template <typename K>
 inline int resident_blocks(K kernel, int threads, size_t smem) {
-    constexpr int kMaxDev = 64;
-    static int cached[kMaxDev][2];     // (threads, blocks) per device; benign race on first use
+    struct Entry {
+        int dev, threads;
+        const void *fn;
+        size_t smem;
+        int blocks;
+    };
+    constexpr int kSlots = 32;
+    static Entry cache[kSlots];
+    static std::mutex mu;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (dev >= 0 && dev < kMaxDev && cached[dev][0] == threads && cached[dev][1] > 0)
-        return cached[dev][1];
+    const void *fn = reinterpret_cast<const void *>(kernel);
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry &e : cache)
+        if (e.blocks > 0 && e.dev == dev && e.fn == fn && e.threads == threads && e.smem == smem)
+            return e.blocks;
     int sms = 0, per_sm = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess)
         return 0;
     const int blocks = sms * (per_sm > 0 ? per_sm : 1);
-    if (dev >= 0 && dev < kMaxDev) {
-        cached[dev][1] = blocks;
-        cached[dev][0] = threads;
-    }
+    for (Entry &e : cache)
+        if (e.blocks == 0) {
+            e = Entry{dev, threads, fn, smem, blocks};
+            break;
+        }
     return blocks;
 }
 
