@@ -66,6 +66,20 @@ def _declare(L):
     L.oracle_e4m3_decode.restype = ctypes.c_float
     L.oracle_layout.argtypes = [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]
     L.oracle_layout.restype = _I
+    L.oracle_rows_max.argtypes = [_I, _I, _I, _I, _I, _L]
+    L.oracle_rows_max.restype = _L
+    L.oracle_layout_padded.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _L, _P, _P, _P, _P, _P]
+    L.oracle_layout_padded.restype = _I
+    L.oracle_fill_padding_rows.argtypes = [_P, _L, _L, _I, _P, _L, _P]
+    L.oracle_fill_padding_rows.restype = None
+    L.oracle_fp8_quantize_row.argtypes = [_P, _I, _P, _P]
+    L.oracle_fp8_quantize_row.restype = None
+    L.oracle_dispatch_fp8.argtypes = [_P, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P]
+    L.oracle_dispatch_fp8.restype = None
+    L.oracle_routing_map_to_topk.argtypes = [_P, _P, _I, _I, _I, _P, _P]
+    L.oracle_routing_map_to_topk.restype = None
+    L.oracle_indices_to_multihot.argtypes = [_P, _P, _I, _I, _I, _P, _P]
+    L.oracle_indices_to_multihot.restype = None
     L.oracle_nvfp4_quantize_row.argtypes = [_P, _I, _P, _P, _P]
     L.oracle_nvfp4_quantize_row.restype = None
     L.oracle_dispatch_nvfp4.argtypes = [_P, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P]
@@ -138,7 +152,8 @@ def e4m3_encode_array(v: np.ndarray) -> np.ndarray:
 # ------------------------------------------------------------------------------------------
 class Layout(dict):
     """Result of :func:`layout`: row_offsets, expert_ids, src_info, row_of, part_tokens, status
-    plus the problem sizes T, K, E, P, C, S and R (rows in use) / R_max (rows allocated)."""
+    plus the problem sizes T, K, E, P, C, S, the padding multiple ``pad`` and R (rows in use,
+    padding included) / R_max (rows allocated)."""
 
     def __getattr__(self, k):
         try:
@@ -147,23 +162,41 @@ class Layout(dict):
             raise AttributeError(k) from e
 
 
-def layout(topk_ids: np.ndarray, E: int, P: int = 1, C: int | None = None, S: int = 0) -> Layout:
+def rows_max(T: int, K: int, E: int, S: int = 0, pad_multiple: int = 1,
+             num_permuted_tokens: int | None = None) -> int:
+    """Rows every dispatched buffer holds: the static capacity when one is given, else the most
+    rows any routing can need, T*K + S*T + G*(pad_multiple - 1)."""
+    return int(lib().oracle_rows_max(T, K, E, S, pad_multiple, num_permuted_tokens or 0))
+
+
+def layout(topk_ids: np.ndarray, E: int, P: int = 1, C: int | None = None, S: int = 0,
+           pad_multiple: int = 1, num_permuted_tokens: int | None = None) -> Layout:
     ids = _c(topk_ids, np.int32)
     T, K = ids.shape
     C = T if C is None else C
     G = E + S
-    R_max = T * K + S * T
+    R_max = rows_max(T, K, E, S, pad_multiple, num_permuted_tokens)
     row_offsets = np.zeros(G + 1, np.int32)
     expert_ids = np.full(max(R_max, 1), -7, np.int32)
     src_info = np.full((max(R_max, 1), 2), -7, np.int32)
     row_of = np.zeros((T, K), np.int32)
     part = np.zeros(P, np.int32)
-    st = lib().oracle_layout(_ptr(ids), T, K, E, P, C, S, _ptr(row_offsets), _ptr(expert_ids),
-                             _ptr(src_info), _ptr(row_of), _ptr(part))
+    st = lib().oracle_layout_padded(_ptr(ids), T, K, E, P, C, S, pad_multiple,
+                                    num_permuted_tokens or 0, _ptr(row_offsets), _ptr(expert_ids),
+                                    _ptr(src_info), _ptr(row_of), _ptr(part))
     R = int(row_offsets[G])
     return Layout(row_offsets=row_offsets, expert_ids=expert_ids[:R_max], src_info=src_info[:R_max],
                   row_of=row_of, part_tokens=part, status=int(st), T=T, K=K, E=E, P=P, C=C, S=S,
-                  R=R, R_max=R_max)
+                  pad=pad_multiple, R=R, R_max=R_max)
+
+
+def _fill_padding(L: Layout, buf: np.ndarray, row: np.ndarray) -> None:
+    """Write ``row`` (the bytes an all-zero token dispatches to) into every padding row."""
+    assert buf.flags.c_contiguous
+    r = np.ascontiguousarray(row).view(np.uint8)
+    src = _c(L.src_info, np.int32)
+    lib().oracle_fill_padding_rows(_ptr(src), L.R, L.R_max, L.status, _ptr(buf.view(np.uint8)),
+                                   r.size, _ptr(r))
 
 
 # ------------------------------------------------------------------------------------------
@@ -192,6 +225,10 @@ def dispatch_nvfp4(x: np.ndarray, L: Layout, fill: int = 0xA5):
     so = np.full(L.E + L.S + 1, -7, np.int32)
     lib().oracle_dispatch_nvfp4(_ptr(x), T, H, L.K, L.E, L.S, _ptr(L.row_offsets), _ptr(L.row_of),
                                 L.status, _ptr(fp4), _ptr(sc), _ptr(inv), _ptr(so))
+    zc, zs, zi = nvfp4_quantize_row(np.zeros(H, np.uint16))
+    _fill_padding(L, fp4, zc)
+    _fill_padding(L, sc, zs)
+    _fill_padding(L, inv, np.array([zi], np.uint16))
     return fp4, sc, inv, so
 
 
@@ -201,7 +238,61 @@ def dispatch_bf16(x: np.ndarray, L: Layout, fill: int = 0xA5A5):
     out = np.full((L.R_max, H), fill, np.uint16)
     lib().oracle_dispatch_bf16(_ptr(x), T, H, L.K, L.E, L.S, _ptr(L.row_offsets), _ptr(L.row_of),
                                L.status, _ptr(out))
+    _fill_padding(L, out, np.zeros(H, np.uint16))
     return out
+
+
+FP8_BLOCK = 128
+
+
+def fp8_quantize_row(x_row: np.ndarray):
+    """(E4M3 codes uint8 [H], float32 scales [H/128]) of one bf16 row."""
+    x = _c(x_row, np.uint16)
+    H = x.size
+    codes = np.zeros(H, np.uint8)
+    scales = np.zeros(H // FP8_BLOCK, np.float32)
+    lib().oracle_fp8_quantize_row(_ptr(x), H, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def dispatch_fp8(x: np.ndarray, L: Layout, fill: int = 0xA5):
+    """FP8 dispatch into buffers of R_max rows pre-filled with ``fill`` bytes."""
+    x = _c(x, np.uint16)
+    T, H = x.shape
+    codes = np.full((L.R_max, H), fill, np.uint8)
+    sc = np.full((L.R_max, 4 * (H // FP8_BLOCK)), fill, np.uint8).view(np.float32)
+    lib().oracle_dispatch_fp8(_ptr(x), T, H, L.K, L.E, L.S, _ptr(L.row_offsets), _ptr(L.row_of),
+                              L.status, _ptr(codes), _ptr(sc))
+    zc, zs = fp8_quantize_row(np.zeros(H, np.uint16))
+    _fill_padding(L, codes, zc)
+    _fill_padding(L, sc, zs)
+    return codes, sc
+
+
+# ------------------------------------------------------------------------------------------
+# routing representations
+# ------------------------------------------------------------------------------------------
+def routing_map_to_topk(routing_map: np.ndarray, dense_probs: np.ndarray | None, K: int):
+    """(topk_ids int32 [T,K], topk_probs float32 [T,K]) from a [T,E] map: ascending expert ids,
+    -1 after the last; a token with more than K experts gets the id E in every slot."""
+    m = _c(routing_map, np.uint8)
+    T, E = m.shape
+    ids = np.zeros((T, K), np.int32)
+    probs = np.zeros((T, K), np.float32)
+    dp = None if dense_probs is None else _c(dense_probs, np.float32)
+    lib().oracle_routing_map_to_topk(_ptr(m), _ptr(dp), T, E, K, _ptr(ids), _ptr(probs))
+    return ids, probs
+
+
+def indices_to_multihot(topk_ids: np.ndarray, topk_probs: np.ndarray | None, E: int):
+    """(routing_map uint8 [T,E], dense_probs float32 [T,E]) from compact ids and probabilities."""
+    ids = _c(topk_ids, np.int32)
+    T, K = ids.shape
+    m = np.zeros((T, E), np.uint8)
+    d = np.zeros((T, E), np.float32)
+    p = None if topk_probs is None else _c(topk_probs, np.float32)
+    lib().oracle_indices_to_multihot(_ptr(ids), _ptr(p), T, K, E, _ptr(m), _ptr(d))
+    return m, d
 
 
 # ------------------------------------------------------------------------------------------
@@ -238,6 +329,7 @@ def combine_bwd(g: np.ndarray, y: np.ndarray, probs: np.ndarray, L: Layout, want
     gy64 = np.zeros((L.R_max, H), np.float64) if want64 else None
     lib().oracle_combine_bwd(_ptr(g), _ptr(y), _ptr(p), T, H, L.K, L.E, L.S, _ptr(L.row_offsets),
                              _ptr(L.row_of), L.status, _ptr(gy), _ptr(gp), _ptr(gy64))
+    _fill_padding(L, gy, np.zeros(H, np.uint16))   # a padding row's gradient is zero
     return (gy, gp, gy64) if want64 else (gy, gp)
 
 

@@ -17,7 +17,10 @@
  * Pins (tests/test_oracle_*.py): brute-force layout invariants, the E2M1 / E4M3 value tables
  * from the format definitions, the 2688 = 6 * 448 closed form, the zero row, the dequantisation
  * error bound, round trips with identity experts, and adjoint identities for both backward
- * passes.  No function here is "parity unpinned".
+ * passes; the padded layout against a row list built by concatenation and hand-worked
+ * examples; FP8 blocks worked by hand, exact power-of-two scaling and the E4M3 error bound;
+ * both routing conversions by brute force over every small map and by round trips.  No
+ * function here is "parity unpinned".
  */
 #include <float.h>
 #include <math.h>
@@ -123,19 +126,30 @@ float oracle_e4m3_decode(uint8_t code)
 
 /* ------------------------------------------------------------------------------------------
  * Layout [Mojo EP dispatch, execute: row_offsets, expert_ids, src_info;
- * fused_a2a, HybridEPDispatch.forward: the rows come out grouped by expert, and an index of
- * -1 routes nowhere; token_dispatcher, _assert_no_hybridep_overflow].
+ * fused_a2a, HybridEPDispatch.forward: the rows come out grouped by expert, an index of -1
+ * routes nowhere, pad_multiple and num_permuted_tokens; token_dispatcher,
+ * TokenDispatcherConfig.moe_router_expert_pad_multiple and _align_up: each expert's token count
+ * is rounded up to a multiple; _assert_no_hybridep_overflow: an overflow flag instead of
+ * silent truncation].
  *
  * 1. An id outside [-1, E) sets BAD_EXPERT and is then treated as an unused slot.
  * 2. counts[e] = #{(t,k): id = e}; with a fused shared expert, group E holds one row per token.
- * 3. row_offsets = exclusive scan of counts over the G = E + S groups; row_offsets[G] = R.
+ * 3. extent[g] = counts[g] rounded up to a multiple of pad (pad = 1: no padding);
+ *    row_offsets = exclusive scan of the extents over the G = E + S groups.
  * 4. Rows of group e are its (t,k) pairs in ascending flat index t*K+k: a stable sort of the
- *    flat indices keyed by expert id.
+ *    flat indices keyed by expert id; the i-th pair of group e is row row_offsets[e] + i.
  * 5. row_of[t*K+k] = row (or -1), src_info[row] = (t, k), expert_ids[row] = e.
  * 6. Shared rows: row_offsets[E] + t, src_info (t, K), expert_ids E.
- * 7. part_tokens[p] = #{t : some id of t lies in partition p = id / (E/P)}; OVERFLOW when any
- *    partition receives more tokens than the capacity C (Mojo EP dispatch, parameter max_token_per_rank).
- * Returns the status bitmask.  The metadata is written in full in every case.
+ * 7. Padding rows row_offsets[g] + counts[g] .. row_offsets[g+1] - 1: expert_ids g,
+ *    src_info (-1, -1).
+ * 8. part_tokens[p] = #{t : some id of t lies in partition p = id / (E/P)}; OVERFLOW when any
+ *    partition receives more tokens than the capacity C (Mojo EP dispatch, parameter
+ *    max_token_per_rank).
+ * 9. Row capacity R_max = row_cap when row_cap > 0 (the static dispatched-token capacity),
+ *    else T*K + S*T + G*(pad-1) (the most rows any routing can need).  OVERFLOW when
+ *    row_offsets[G] > R_max; a row at or past R_max is not recorded: its src_info and
+ *    expert_ids are not written and row_of of its pair is -1.
+ * Returns the status bitmask.  Apart from step 9 the metadata is written in full in every case.
  * ---------------------------------------------------------------------------------------- */
 typedef struct { int32_t e; int32_t i; } sort_key;
 
@@ -147,13 +161,21 @@ static int cmp_key(const void *pa, const void *pb)
     return a->i < b->i ? -1 : (a->i > b->i);
 }
 
-int oracle_layout(const int32_t *topk_ids, int T, int K, int E, int P, int C, int S,
-                  int32_t *row_offsets, int32_t *expert_ids, int32_t *src_info,
-                  int32_t *row_of, int32_t *part_tokens)
+long oracle_rows_max(int T, int K, int E, int S, int pad, long row_cap)
+{
+    if (row_cap > 0)
+        return row_cap;
+    return (long)T * K + (long)S * T + (long)(E + S) * (pad - 1);
+}
+
+int oracle_layout_padded(const int32_t *topk_ids, int T, int K, int E, int P, int C, int S,
+                         int pad, long row_cap, int32_t *row_offsets, int32_t *expert_ids,
+                         int32_t *src_info, int32_t *row_of, int32_t *part_tokens)
 {
     int status = 0;
     long n = (long)T * K;
     int G = E + S;
+    long R_max = oracle_rows_max(T, K, E, S, pad, row_cap);
     int32_t *id = malloc(sizeof(int32_t) * (n ? n : 1));
     for (long i = 0; i < n; i++) {
         int32_t v = topk_ids[i];
@@ -174,9 +196,11 @@ int oracle_layout(const int32_t *topk_ids, int T, int K, int E, int P, int C, in
     long acc = 0;
     for (int g = 0; g < G; g++) {
         row_offsets[g] = (int32_t)acc;
-        acc += counts[g];
+        acc += (counts[g] + pad - 1) / pad * pad;
     }
     row_offsets[G] = (int32_t)acc;
+    if (acc > R_max)
+        status |= ORC_OVERFLOW;
 
     sort_key *keys = malloc(sizeof(sort_key) * (n ? n : 1));
     long nv = 0;
@@ -189,19 +213,38 @@ int oracle_layout(const int32_t *topk_ids, int T, int K, int E, int P, int C, in
         }
     }
     qsort(keys, (size_t)nv, sizeof(sort_key), cmp_key);   /* (e, i) keys are distinct: stable */
-    for (long r = 0; r < nv; r++) {
-        int32_t i = keys[r].i;
-        row_of[i] = (int32_t)r;
-        src_info[2 * r] = i / K;
-        src_info[2 * r + 1] = i % K;
-        expert_ids[r] = keys[r].e;
+    long j = 0;
+    while (j < nv) {   /* one run of equal experts at a time */
+        int e = keys[j].e;
+        long first = j;
+        for (; j < nv && keys[j].e == e; j++) {
+            long r = row_offsets[e] + (j - first);
+            if (r >= R_max)
+                continue;
+            int32_t i = keys[j].i;
+            row_of[i] = (int32_t)r;
+            src_info[2 * r] = i / K;
+            src_info[2 * r + 1] = i % K;
+            expert_ids[r] = e;
+        }
     }
     if (S) {
         for (int t = 0; t < T; t++) {
             long r = row_offsets[E] + t;
+            if (r >= R_max)
+                continue;
             src_info[2 * r] = t;
             src_info[2 * r + 1] = K;
             expert_ids[r] = E;
+        }
+    }
+    for (int g = 0; g < G; g++) {
+        for (long r = row_offsets[g] + counts[g]; r < row_offsets[g + 1]; r++) {
+            if (r >= R_max)
+                continue;
+            src_info[2 * r] = -1;
+            src_info[2 * r + 1] = -1;
+            expert_ids[r] = g;
         }
     }
 
@@ -225,6 +268,15 @@ int oracle_layout(const int32_t *topk_ids, int T, int K, int E, int P, int C, in
     free(counts);
     free(id);
     return status;
+}
+
+/* The layout without padding or a row capacity (pad = 1, R_max = T*K + S*T). */
+int oracle_layout(const int32_t *topk_ids, int T, int K, int E, int P, int C, int S,
+                  int32_t *row_offsets, int32_t *expert_ids, int32_t *src_info,
+                  int32_t *row_of, int32_t *part_tokens)
+{
+    return oracle_layout_padded(topk_ids, T, K, E, P, C, S, 1, 0, row_offsets, expert_ids,
+                                src_info, row_of, part_tokens);
 }
 
 /* ------------------------------------------------------------------------------------------
@@ -455,4 +507,151 @@ void oracle_e4m3_encode_n(const float *v, uint8_t *codes, long n)
 {
     for (long i = 0; i < n; i++)
         codes[i] = oracle_e4m3_encode(v[i]);
+}
+
+/* ------------------------------------------------------------------------------------------
+ * Padding rows of a dispatched buffer [token_dispatcher,
+ * TokenDispatcherConfig.moe_router_expert_pad_multiple: the tokens an expert's count is padded
+ * with; fused_a2a, HybridEPDispatch.forward pad_multiple].  A padding token is an all-zero
+ * token: every padding row (src_info token -1) below min(row_offsets[G], R_max) receives
+ * `row`, the row_bytes bytes that the dispatch writes for an all-zero token.  Writes nothing
+ * when status != 0.
+ * ---------------------------------------------------------------------------------------- */
+void oracle_fill_padding_rows(const int32_t *src_info, long R_pad, long R_max, int status,
+                              uint8_t *buf, long row_bytes, const uint8_t *row)
+{
+    if (status)
+        return;
+    long end = R_pad < R_max ? R_pad : R_max;
+    for (long r = 0; r < end; r++)
+        if (src_info[2 * r] < 0)
+            memcpy(buf + (size_t)r * (size_t)row_bytes, row, (size_t)row_bytes);
+}
+
+/* ------------------------------------------------------------------------------------------
+ * FP8 quantisation of one token [fused_a2a, init_hybrid_ep_buffer, fp8_dispatch: the
+ * dispatch may carry FP8 instead of BF16; the pages fix no block size or scale format].  E4M3 codes with one binary32 scale per block of
+ * 128 consecutive elements; every operation in binary32, rounded once:
+ *   ab = max |x| over the block
+ *   s  = 1 if ab == 0, else 448 / ab (clamped to FLT_MAX if that overflows)
+ *   code = E4M3(x * s)                    (round to nearest even, saturating to +-448)
+ *   scale = 1 / s                         (what a consumer multiplies the codes by)
+ * so the block's largest magnitude lands on E4M3's largest finite value.
+ * ---------------------------------------------------------------------------------------- */
+#define ORC_FP8_BLOCK 128
+
+void oracle_fp8_quantize_row(const uint16_t *x, int H, uint8_t *codes, float *scales)
+{
+    for (int b = 0; b < H / ORC_FP8_BLOCK; b++) {
+        const uint16_t *xb = x + ORC_FP8_BLOCK * b;
+        float ab = 0.0f;
+        for (int i = 0; i < ORC_FP8_BLOCK; i++) {
+            float v = fabsf((float)oracle_bf16_to_double(xb[i]));
+            if (v > ab)
+                ab = v;
+        }
+        float s = 1.0f;
+        if (ab != 0.0f) {
+            s = 448.0f / ab;
+            if (isinf(s))
+                s = FLT_MAX;
+        }
+        scales[b] = 1.0f / s;
+        for (int i = 0; i < ORC_FP8_BLOCK; i++) {
+            float y = (float)oracle_bf16_to_double(xb[i]) * s;
+            codes[ORC_FP8_BLOCK * b + i] = oracle_e4m3_encode(y);
+        }
+    }
+}
+
+/* FP8 dispatch: every row of token t (its K routed copies and the shared copy) receives the
+ * same codes and block scales.  Writes nothing when status != 0. */
+void oracle_dispatch_fp8(const uint16_t *x, int T, int H, int K, int E, int S,
+                         const int32_t *row_offsets, const int32_t *row_of, int status,
+                         uint8_t *out_codes, float *out_scales)
+{
+    if (status)
+        return;
+    int nb = H / ORC_FP8_BLOCK;
+    uint8_t *codes = malloc((size_t)H);
+    float *sc = malloc(sizeof(float) * (size_t)nb);
+    for (int t = 0; t < T; t++) {
+        oracle_fp8_quantize_row(x + (size_t)t * H, H, codes, sc);
+        for (int k = 0; k <= K; k++) {
+            long r;
+            if (k < K)
+                r = row_of[(long)t * K + k];
+            else
+                r = S ? (long)row_offsets[E] + t : -1;
+            if (r < 0)
+                continue;
+            memcpy(out_codes + (size_t)r * H, codes, (size_t)H);
+            memcpy(out_scales + (size_t)r * nb, sc, sizeof(float) * (size_t)nb);
+        }
+    }
+    free(sc);
+    free(codes);
+}
+
+/* ------------------------------------------------------------------------------------------
+ * Routing representations [fused_a2a, HybridEPDispatch.forward: a dense Boolean routing map
+ * [tokens, experts] or compact top-k indices [tokens, top_k] with -1 for an unused slot, the
+ * map taking precedence, the probabilities staying dense; token_dispatcher,
+ * _DeepepManager._indices_to_multihot / _HybridEPManager._indices_to_multihot].
+ *
+ * Map -> compact: slot j of token t holds the j-th expert (ascending id) whose map entry is
+ * non-zero, and its dense probability; the slots after the last one hold -1 and probability 0.
+ * A token with more than K experts in its map cannot be written in K slots: all its slots get
+ * the id E (outside [-1, E), so the layout that reads them reports BAD_EXPERT) and
+ * probability 0.  dense_probs / topk_probs may be NULL (no probabilities).
+ * ---------------------------------------------------------------------------------------- */
+void oracle_routing_map_to_topk(const uint8_t *routing_map, const float *dense_probs, int T,
+                                int E, int K, int32_t *topk_ids, float *topk_probs)
+{
+    for (int t = 0; t < T; t++) {
+        int n = 0;
+        for (int e = 0; e < E; e++)
+            if (routing_map[(long)t * E + e])
+                n++;
+        int j = 0;
+        for (int e = 0; e < E && n <= K; e++) {
+            if (!routing_map[(long)t * E + e])
+                continue;
+            topk_ids[(long)t * K + j] = e;
+            if (topk_probs)
+                topk_probs[(long)t * K + j] = dense_probs ? dense_probs[(long)t * E + e] : 0.0f;
+            j++;
+        }
+        for (int k = (n <= K ? n : 0); k < K; k++) {
+            topk_ids[(long)t * K + k] = n <= K ? -1 : E;
+            if (topk_probs)
+                topk_probs[(long)t * K + k] = 0.0f;
+        }
+    }
+}
+
+/* Compact -> map: routing_map[t,e] = 1 when some slot of t holds e, else 0; dense[t,e] = the
+ * binary32 sum, over those slots in ascending k and starting from +0, of their probabilities
+ * (a token naming an expert twice sends it the sum).  Ids outside [0, E) are skipped: they
+ * route nowhere here (the layout is what reports ids outside [-1, E)).  topk_probs /
+ * dense_probs may be NULL. */
+void oracle_indices_to_multihot(const int32_t *topk_ids, const float *topk_probs, int T, int K,
+                                int E, uint8_t *routing_map, float *dense_probs)
+{
+    for (int t = 0; t < T; t++) {
+        for (int e = 0; e < E; e++) {
+            uint8_t hit = 0;
+            float acc = 0.0f;
+            for (int k = 0; k < K; k++) {
+                if (topk_ids[(long)t * K + k] != e)
+                    continue;
+                hit = 1;
+                if (topk_probs)
+                    acc = acc + topk_probs[(long)t * K + k];
+            }
+            routing_map[(long)t * E + e] = hit;
+            if (dense_probs)
+                dense_probs[(long)t * E + e] = acc;
+        }
+    }
 }

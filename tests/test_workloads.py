@@ -5,7 +5,7 @@ import pytest
 import workloads as W
 
 
-@pytest.mark.parametrize("name", ["tiny", "qwen3", "dsv3", "mixtral"])
+@pytest.mark.parametrize("name", ["tiny", "qwen3", "dsv3", "mixtral", "dsv3_static"])
 def test_routing_shapes_distinct_and_normalised(name):
     cfg = W.CONFIGS[name]
     cfg = W.scaled(cfg, T=min(cfg.T, 512))
@@ -42,3 +42,16 @@ def test_x_structure():
 def test_bf16_rounding_of_generator():
     v = np.array([1.0, 1 + 2 ** -8, 1 + 3 * 2 ** -8, -0.0, 3.0e38], np.float32)
     assert W.bf16_bits_from_f32(v).tolist() == [0x3F80, 0x3F80, 0x3F82, 0x8000, 0x7F62]
+
+
+def test_static_routing_is_balanced_and_fills_its_capacity():
+    import oracle
+    cfg = W.CONFIGS["dsv3_static"]
+    ids, p = W.make_routing(cfg)
+    counts = np.bincount(ids.ravel(), minlength=cfg.E)
+    assert (counts == cfg.T * cfg.K // cfg.E).all()
+    assert (p == np.float32(1.0 / cfg.K)).all()
+    L = oracle.layout(ids[:512], cfg.E, P=cfg.P, C=cfg.capacity, S=cfg.S, pad_multiple=16,
+                      num_permuted_tokens=512 * cfg.K + 512)
+    assert L.status == 0 and L.R == L.R_max          # every group a multiple of 16: no padding
+    assert (L.part_tokens == 512 // cfg.P).all()     # each token's 8 experts share a partition

@@ -16,6 +16,9 @@ Recipe (all draws from ``numpy.random.Generator(PCG64(seed))``):
   probabilities computed in float64 and rounded to float32;
 * expert outputs ``y`` and gradients: standard normal in float32 rounded to bf16.
 
+The "balanced" router draws nothing: slot k of token t names expert (t*K + k) mod E with
+probability 1/K (static routing for benchmarks, so every dispatch permutes the same row count).
+
 Seeds per config index c: x 1000+c, logits 2000+c, expert bias 3000+c, Zipf draws 4000+c,
 outlier / zero-row choice 5000+c, grad_out 6000+c, expert outputs 7000+c, grad rows 8000+c.
 """
@@ -46,10 +49,12 @@ class Config:
     S: int = 0
     P: int = 1
     C: int | None = None          # None: capacity = T (never overflows)
-    router: str = "softmax"       # softmax | dsv3 | zipf | hot
+    router: str = "softmax"       # softmax | dsv3 | zipf | hot | balanced
     outlier_frac: float = 0.0     # fraction of rows scaled x50
     zero_frac: float = 0.0        # fraction of all-zero rows
     rerun_C: int | None = None    # capacity of the full rerun after an overflow run
+    pad_multiple: int = 1         # rows of every group padded to a multiple of this
+    num_permuted_tokens: int | None = None   # static row capacity (None: the most any routing needs)
 
     @property
     def capacity(self) -> int:
@@ -63,6 +68,10 @@ CONFIGS: dict[str, Config] = {
     "mixtral": Config(4, "mixtral", T=16384, H=4096, E=8, K=2, router="zipf"),
     "dsv3_large": Config(5, "dsv3_large", T=32768, H=7168, E=256, K=8, P=8, C=20000,
                          router="hot", zero_frac=0.001, rerun_C=40000),
+    # benchmark static routing: forced-balanced, no noise, so every dispatch has the same row
+    # count (T*K/E = 128 rows per expert), passed as a static row capacity; groups padded to 128
+    "dsv3_static": Config(6, "dsv3_static", T=4096, H=7168, E=256, K=8, S=1, P=8, C=4096,
+                          router="balanced", pad_multiple=128, num_permuted_tokens=4096 * 8 + 4096),
 }
 
 
@@ -178,6 +187,14 @@ def make_routing(cfg: Config) -> tuple[np.ndarray, np.ndarray]:
         probs = _softmax_rows(logits)
         return ids.astype(np.int32), probs.astype(np.float32)
 
+    if cfg.router == "balanced":
+        # slot k of token t names expert (t*K + k) mod E: K distinct experts per token (K <= E)
+        # and, when E divides T*K, exactly T*K/E rows per expert; equal probabilities 1/K
+        t = np.arange(T, dtype=np.int64)[:, None]
+        k = np.arange(K, dtype=np.int64)[None, :]
+        ids = (t * K + k) % E
+        probs = np.full((T, K), 1.0 / K)
+        return ids.astype(np.int32), probs.astype(np.float32)
     logits = _rng(2000 + c).standard_normal((T, E))
     if cfg.router == "dsv3":
         bias = 0.5 * _rng(3000 + c).standard_normal(E)
