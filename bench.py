@@ -64,7 +64,20 @@ def algorithmic_bytes(cfg: W.Config, R: int) -> dict:
         "dispatch_bf16": 2 * T * H + 2 * R * H + 4 * T * K,
         "combine_bwd": 2 * T * H + 2 * routed * H + 2 * R * H + 12 * T * K,
         "dispatch_bwd": 2 * R * H + 4 * T * K + 2 * T * H,
+        "dispatch_fp8": 2 * T * H + R * (H + 4 * (H // 128)),
+        # dense routing map in (T*E bytes + T*E fp32 probabilities), compact ids / probs out,
+        # then the layout of those ids
+        "routing_map_layout": 5 * T * cfg.E + 8 * T * K + (4 * T * K + 12 * R + 4 * T * K),
+        "indices_to_multihot": 8 * T * K + 5 * T * cfg.E,
     }
+
+
+def padded_bytes(cfg: W.Config, R_pad: int) -> dict:
+    """Layout and NVFP4 dispatch of a padded layout: every row below R_pad (padding rows
+    included) is written once."""
+    T, H, K = cfg.T, cfg.H, cfg.K
+    return {"layout": 4 * T * K + 12 * R_pad + 4 * T * K,
+            "dispatch_nvfp4": 2 * T * H + R_pad * (H // 2 + H // 16 + 2)}
 
 
 def load_peaks() -> tuple[float, str]:
@@ -362,10 +375,39 @@ def run_ours(args, cfg):
     g_rows = torch.empty(R_max, H, dtype=torch.bfloat16, device=dev)
     g_probs = torch.empty(T, K, dtype=torch.float32, device=dev)
     g_x = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    fp8_codes = torch.empty(R_max, H, dtype=torch.uint8, device=dev)
+    fp8_scales = torch.empty(R_max, H // 128, dtype=torch.float32, device=dev)
+    # the same routing as a dense map [T, E] with dense probabilities
+    rmap, dprobs = ep.indices_to_multihot(ids, probs, E)
+    Lm = ep.Layout(T, K, E, P, bool(S), device=dev)
+    map_ids = torch.empty(T, K, dtype=torch.int32, device=dev)
+    map_probs = torch.empty(T, K, dtype=torch.float32, device=dev)
+    mh_map = torch.empty(T, E, dtype=torch.uint8, device=dev)
+    mh_dense = torch.empty(T, E, dtype=torch.float32, device=dev)
+    # groups padded to 128 rows (a grouped-GEMM tile), buffers sized for the padded rows
+    PAD = 128
+    Lp = ep.Layout(T, K, E, P, bool(S), device=dev, pad_multiple=PAD)
+    p_fp4 = torch.empty(Lp.R_max, H // 2, dtype=torch.uint8, device=dev)
+    p_sc = torch.empty(Lp.R_max, H // 16, dtype=torch.uint8, device=dev)
+    p_inv = torch.empty(Lp.R_max, dtype=torch.bfloat16, device=dev)
+    p_so = torch.empty(E + S + 1, dtype=torch.int32, device=dev)
+    ep.dispatch_layout_routed(E, topk_ids=ids, n_parts=P, capacity=C, fused_shared=bool(S),
+                              pad_multiple=PAD, out=Lp, stream=stream)
     extra_fns = {
         "dispatch_bf16": lambda: ep.dispatch_bf16(x, L, out=rows_bf16, stream=stream),
         "combine_bwd": lambda: ep.combine_bwd(g_out, y, probs, L, out=(g_rows, g_probs), stream=stream),
         "dispatch_bwd": lambda: ep.dispatch_bwd(y, L, out=g_x, stream=stream),
+        "dispatch_fp8": lambda: ep.dispatch_fp8(x, L, out=(fp8_codes, fp8_scales), stream=stream),
+        "routing_map_layout": lambda: ep.dispatch_layout_routed(
+            E, routing_map=rmap, dense_probs=dprobs, K=K, n_parts=P, capacity=C, fused_shared=bool(S),
+            out=Lm, map_out=(map_ids, map_probs), stream=stream),
+        "indices_to_multihot": lambda: ep.indices_to_multihot(ids, probs, E, out=(mh_map, mh_dense),
+                                                              stream=stream),
+        f"layout (pad {PAD})": lambda: ep.dispatch_layout_routed(
+            E, topk_ids=ids, n_parts=P, capacity=C, fused_shared=bool(S), pad_multiple=PAD, out=Lp,
+            stream=stream),
+        f"dispatch_nvfp4 (pad {PAD})": lambda: ep.dispatch_nvfp4(x, Lp, out=(p_fp4, p_sc, p_inv, p_so),
+                                                                 stream=stream),
     }
     extra = {}
     for name, fn in extra_fns.items():
@@ -381,6 +423,12 @@ def run_ours(args, cfg):
             b.record(stream)
         torch.cuda.synchronize(dev)
         extra[name] = float(np.mean([a.elapsed_time(b) for a, b in pairs])) * 1e-3
+
+    torch.cuda.synchronize(dev)
+    if ep.read_status(Lp) != 0 or ep.read_status(Lm) != 0:
+        raise RuntimeError("padded or routing-map layout reported an error on the benchmark workload")
+    R_pad = int(Lp.row_offsets[Lp.G].item())
+    static = static_routing_step(ep, dev, stream, flush_l2, nb)
 
     # ---- e2e through the public API with pinned host buffers ----
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
@@ -431,6 +479,9 @@ def run_ours(args, cfg):
         return 0
 
     ab = algorithmic_bytes(cfg, R)
+    pb = padded_bytes(cfg, R_pad)
+    ab[f"layout (pad {PAD})"] = pb["layout"]
+    ab[f"dispatch_nvfp4 (pad {PAD})"] = pb["dispatch_nvfp4"]
     peak, peak_kind = load_peaks()
     achieved = ab["combine"] / comb_s / 1e9
     traffic = recorded_traffic("combine")
@@ -460,9 +511,14 @@ def run_ours(args, cfg):
         "kernels": kernels,
         "kernels_note": (f"layout, dispatch_nvfp4 and combine: mean of {nb} diagnostic steps after the "
                          "timed region that call ep_dispatch_layout and ep_dispatch_nvfp4 separately, "
-                         "events between kernels; the fused call from the timed steps; "
-                         "dispatch_bf16, combine_bwd and dispatch_bwd (not in the step) timed alone on "
-                         "the same layout, L2 flushed before each launch"),
+                         "events between kernels; the fused call from the timed steps; the other "
+                         "entries (not in the step) timed alone on the same routing, L2 flushed before "
+                         f"each call: dispatch_bf16, combine_bwd, dispatch_bwd, dispatch_fp8, the layout "
+                         f"from the routing as a dense map (map -> ids, then the layout), "
+                         f"indices_to_multihot, and the layout and NVFP4 dispatch with groups padded to "
+                         f"{PAD} rows ({R_pad} rows, {R_pad - R} of them padding, written as an "
+                         f"all-zero token)"),
+        "static_routing_step": static,
         "e2e": {"value": ws * T * e2e_steps / e2e_t, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "path": "pinned host x/ids/probs/expert outputs -> device, layout + NVFP4 dispatch + "
@@ -481,6 +537,61 @@ def run_ours(args, cfg):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def static_routing_step(ep, dev, stream, flush_l2, n_steps: int) -> dict:
+    """Layout + NVFP4 dispatch + combine on the forced-balanced static routing workload, with its
+    persisted row count passed as the static row capacity and groups padded to 128 rows; L2
+    flushed before each step, events around it."""
+    import torch
+    cfg = W.CONFIGS["dsv3_static"]
+    T, H, E, K, S, P, C = cfg.T, cfg.H, cfg.E, cfg.K, cfg.S, cfg.P, cfg.capacity
+    inp = W.make_inputs(cfg)
+    x = torch.from_numpy(inp["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+    ids = torch.from_numpy(inp["topk_ids"]).to(dev)
+    probs = torch.from_numpy(inp["probs"]).to(dev)
+    Ls = ep.Layout(T, K, E, P, bool(S), device=dev, pad_multiple=cfg.pad_multiple,
+                   num_permuted_tokens=cfg.num_permuted_tokens)
+    Rm = Ls.R_max
+    y = torch.from_numpy(np.resize(W.make_expert_out(cfg), (Rm, H)).view(np.int16)).to(dev).view(torch.bfloat16)
+    fp4 = torch.empty(Rm, H // 2, dtype=torch.uint8, device=dev)
+    sc = torch.empty(Rm, H // 16, dtype=torch.uint8, device=dev)
+    inv = torch.empty(Rm, dtype=torch.bfloat16, device=dev)
+    so = torch.empty(E + S + 1, dtype=torch.int32, device=dev)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+
+    def step():
+        ep.dispatch_layout_routed(E, topk_ids=ids, n_parts=P, capacity=C, fused_shared=bool(S),
+                                  pad_multiple=cfg.pad_multiple,
+                                  num_permuted_tokens=cfg.num_permuted_tokens, out=Ls, stream=stream)
+        ep.dispatch_nvfp4(x, Ls, out=(fp4, sc, inv, so), stream=stream)
+        ep.combine(y, probs, Ls, out=out, stream=stream)
+
+    step()
+    torch.cuda.synchronize(dev)
+    if ep.read_status(Ls) != 0:
+        raise RuntimeError("static routing layout reported an error")
+    R = int(Ls.row_offsets[Ls.G].item())
+    for _ in range(3):
+        flush_l2()
+        step()
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(n_steps)]
+    for a, b in pairs:
+        flush_l2()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    sec = float(np.mean([a.elapsed_time(b) for a, b in pairs])) * 1e-3
+    ab = algorithmic_bytes(cfg, R)
+    nbytes = ab["layout"] + ab["dispatch_nvfp4"] + ab["combine"]
+    return {"workload": f"{cfg.name}: T={T}, hidden={H}, {E} experts, top-{K}, shared expert, "
+                        f"balanced routing ({T * K // E} rows per expert), pad {cfg.pad_multiple}, "
+                        f"static row capacity {cfg.num_permuted_tokens}",
+            "us_per_step": sec * 1e6, "tokens/s": T / sec, "rows": R, "algorithmic_bytes": nbytes,
+            "GB/s": nbytes / sec / 1e9, "steps": n_steps,
+            "calls": "ep_dispatch_layout_routed + ep_dispatch_nvfp4 (+ padding fill) + ep_combine"}
 
 
 def main():

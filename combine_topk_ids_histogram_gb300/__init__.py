@@ -6,9 +6,10 @@ runs in the library's CUDA kernels.  There is no CPU fallback: importing the bin
 the built library raises.
 
 Entry points (same names as the C ABI, without the ``ep_`` prefix):
-``dispatch_layout``, ``dispatch_nvfp4``, ``dispatch_layout_nvfp4``, ``dispatch_bf16``, ``combine``,
-``combine_bwd``,
-``dispatch_bwd``, ``read_status``, ``cvt_e2m1``, ``cvt_e4m3``.
+``dispatch_layout``, ``dispatch_layout_routed``, ``dispatch_layout_noalloc``, ``dispatch_nvfp4``,
+``dispatch_layout_nvfp4``, ``dispatch_bf16``, ``dispatch_fp8``, ``combine``, ``combine_bwd``,
+``dispatch_bwd``, ``routing_map_to_topk``, ``indices_to_multihot``, ``rows_max``,
+``read_status``, ``cvt_e2m1``, ``cvt_e4m3``.
 """
 from __future__ import annotations
 
@@ -53,6 +54,8 @@ class _Layout(ctypes.Structure):
         ("P", ctypes.c_int),
         ("capacity", ctypes.c_int),
         ("fused_shared", ctypes.c_int),
+        ("pad_multiple", ctypes.c_int),
+        ("row_capacity", ctypes.c_int),
     ]
 
 
@@ -62,7 +65,12 @@ _LP = ctypes.POINTER(_Layout)
 # name -> (restype, argtypes); must match include/ep.h
 SIGNATURES = {
     "ep_layout_workspace_bytes": (_Z, [_I, _I, _I, _I]),
+    "ep_rows_max": (_Z, [_I, _I, _I, _I, _I, _I]),
     "ep_dispatch_layout": (_I, [_P, _I, _I, _I, _I, _I, _I, _LP, _P]),
+    "ep_dispatch_layout_routed": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _LP, _P]),
+    "ep_routing_map_to_topk": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
+    "ep_indices_to_multihot": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
+    "ep_dispatch_fp8": (_I, [_P, _I, _LP, _P, _P, _P]),
     "ep_dispatch_layout_noalloc": (_I, [_P, _I, _I, _I, _I, _I, _I, _LP, _P]),
     "ep_dispatch_nvfp4": (_I, [_P, _I, _LP, _P, _P, _P, _P, _P]),
     "ep_dispatch_layout_nvfp4": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _I, _LP, _P, _P, _P, _P, _P]),
@@ -149,22 +157,36 @@ def layout_workspace_bytes(T: int, K: int, n_experts: int, fused_shared: bool = 
     return int(_lib.ep_layout_workspace_bytes(T, K, n_experts, int(bool(fused_shared))))
 
 
+def rows_max(T: int, K: int, n_experts: int, fused_shared: bool = False, pad_multiple: int = 1,
+             num_permuted_tokens: int | None = None) -> int:
+    """ep_rows_max: rows every dispatched buffer holds (the static capacity when one is given,
+    else T*K + S*T + G*(pad_multiple - 1))."""
+    n = int(_lib.ep_rows_max(T, K, n_experts, int(bool(fused_shared)), pad_multiple,
+                             int(num_permuted_tokens or 0)))
+    if n == 0 and T * K > 0:
+        raise EPError(EP_ERR_INVALID_ARG, "rows_max sizes")
+    return n
+
+
 class Layout:
     """Device buffers of one dispatch layout (see ``ep_layout_t`` in include/ep.h).
 
     ``row_offsets`` [G+1], ``expert_ids`` [R_max], ``src_info`` [R_max, 2], ``row_of`` [T, K],
     ``part_tokens`` [P], ``status`` [1] and the zero-initialised ``workspace``; all int32
-    except the workspace (uint8).  The buffers are allocated once for a shape and reused by
-    every ``dispatch_layout`` call into this object.
+    except the workspace (uint8).  The buffers are allocated once for a shape (including the
+    padding multiple and the static row capacity, which set R_max) and reused by every layout
+    call into this object.
     """
 
     def __init__(self, T: int, K: int, n_experts: int, n_parts: int = 1, fused_shared: bool = False,
-                 device=None):
+                 device=None, pad_multiple: int = 1, num_permuted_tokens: int | None = None):
         dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
         S = int(bool(fused_shared))
         self.T, self.K, self.E, self.P, self.S = T, K, n_experts, n_parts, S
         self.G = n_experts + S
-        self.R_max = T * K + S * T
+        self.pad = int(pad_multiple)
+        self.row_capacity = int(num_permuted_tokens or 0)
+        self.R_max = rows_max(T, K, n_experts, S, self.pad, self.row_capacity)
         i32 = dict(dtype=torch.int32, device=dev)
         self.row_offsets = torch.empty(self.G + 1, **i32)
         self.expert_ids = torch.empty(max(self.R_max, 1), **i32)
@@ -187,6 +209,9 @@ class Layout:
     def ref(self):
         return ctypes.byref(self.c)
 
+    def shape_key(self):
+        return (self.T, self.K, self.E, self.P, self.S, self.pad, self.row_capacity)
+
     def num_rows(self) -> torch.Tensor:
         """R as a device tensor (no host sync)."""
         return self.row_offsets[self.G]
@@ -199,10 +224,8 @@ def dispatch_layout(topk_ids: torch.Tensor, n_experts: int, n_parts: int = 1,
     if topk_ids.dtype != torch.int32 or topk_ids.dim() != 2:
         raise TypeError("topk_ids must be an int32 [T, K] tensor")
     T, K = topk_ids.shape
-    if out is not None and (out.T, out.K, out.E, out.P, out.S) != (T, K, n_experts, n_parts,
-                                                                    int(bool(fused_shared))):
-        raise ValueError("layout buffers were allocated for other sizes "
-                         f"{(out.T, out.K, out.E, out.P, out.S)}")
+    if out is not None and out.shape_key() != (T, K, n_experts, n_parts, int(bool(fused_shared)), 1, 0):
+        raise ValueError(f"layout buffers were allocated for other sizes {out.shape_key()}")
     L = out if out is not None else Layout(T, K, n_experts, n_parts, fused_shared, topk_ids.device)
     cap = T if capacity is None else int(capacity)
     L.capacity = cap
@@ -225,14 +248,135 @@ def dispatch_layout_noalloc(topk_ids: torch.Tensor, n_experts: int, n_parts: int
     if out is None:
         raise ValueError("dispatch_layout_noalloc writes into caller-provided buffers: pass out=")
     T, K = topk_ids.shape
-    if (out.T, out.K, out.E, out.P, out.S) != (T, K, n_experts, n_parts, int(bool(fused_shared))):
-        raise ValueError("layout buffers were allocated for other sizes "
-                         f"{(out.T, out.K, out.E, out.P, out.S)}")
+    if out.shape_key() != (T, K, n_experts, n_parts, int(bool(fused_shared)), 1, 0):
+        raise ValueError(f"layout buffers were allocated for other sizes {out.shape_key()}")
     cap = T if capacity is None else int(capacity)
     out.capacity = cap
     rc = _lib.ep_dispatch_layout_noalloc(_ptr(topk_ids) if T > 0 else None, T, K, n_experts, n_parts,
                                          cap, int(bool(fused_shared)), out.ref, _stream(stream))
     _check(rc, "ep_dispatch_layout_noalloc")
+    return out
+
+
+def dispatch_layout_routed(n_experts: int, topk_ids: torch.Tensor | None = None,
+                           routing_map: torch.Tensor | None = None,
+                           dense_probs: torch.Tensor | None = None, K: int | None = None,
+                           n_parts: int = 1, capacity: int | None = None,
+                           fused_shared: bool = False, pad_multiple: int = 1,
+                           num_permuted_tokens: int | None = None, out: Layout | None = None,
+                           map_out=None, stream=None):
+    """ep_dispatch_layout_routed: the layout from compact ids [T, K] or from a dense routing map
+    [T, E] (uint8 / bool, which takes precedence when both are given, with optional dense
+    probabilities [T, E] fp32), with groups padded to ``pad_multiple`` rows and an optional
+    static row capacity ``num_permuted_tokens``.  Returns (Layout, topk_ids, topk_probs): the
+    compact ids the layout was made from (the converted map when one was given) and, for a map
+    with dense probabilities, the per-slot probabilities combine takes (else None)."""
+    if routing_map is not None:
+        if routing_map.dtype not in (torch.uint8, torch.bool) or routing_map.dim() != 2:
+            raise TypeError("routing_map must be a uint8 / bool [T, E] tensor")
+        T, E = routing_map.shape
+        if E != n_experts:
+            raise ValueError("routing_map has the wrong number of experts")
+        if K is None:
+            K = topk_ids.shape[1] if topk_ids is not None else None
+        if K is None:
+            raise ValueError("K (slots per token) is needed with a routing map")
+        if dense_probs is not None:
+            _need(dense_probs, None, E, (torch.float32,), "dense_probs", exact_rows=T)
+        dev = routing_map.device
+        if map_out is None:
+            map_out = (torch.empty(max(T, 1), K, dtype=torch.int32, device=dev),
+                       torch.empty(max(T, 1), K, dtype=torch.float32, device=dev)
+                       if dense_probs is not None else None)
+        ids, probs = map_out
+        _need(ids, T, K, (torch.int32,), "map_topk_ids")
+        if probs is not None:
+            _need(probs, T, K, (torch.float32,), "map_topk_probs")
+        rmap = routing_map.view(torch.uint8) if routing_map.dtype == torch.bool else routing_map
+    else:
+        if topk_ids is None or topk_ids.dtype != torch.int32 or topk_ids.dim() != 2:
+            raise TypeError("topk_ids must be an int32 [T, K] tensor when no routing_map is given")
+        T, K = topk_ids.shape
+        ids, probs, rmap = topk_ids, None, None
+        dev = topk_ids.device
+    S = int(bool(fused_shared))
+    key = (T, K, n_experts, n_parts, S, int(pad_multiple), int(num_permuted_tokens or 0))
+    if out is not None and out.shape_key() != key:
+        raise ValueError(f"layout buffers were allocated for other sizes {out.shape_key()}")
+    L = out if out is not None else Layout(T, K, n_experts, n_parts, fused_shared, dev,
+                                           pad_multiple, num_permuted_tokens)
+    cap = T if capacity is None else int(capacity)
+    L.capacity = cap
+    rc = _lib.ep_dispatch_layout_routed(
+        _ptr(topk_ids) if (rmap is None and T > 0) else None,
+        _ptr(rmap) if (rmap is not None and T > 0) else None,
+        _ptr(dense_probs) if (rmap is not None and T > 0) else None,
+        T, K, n_experts, n_parts, cap, S, int(pad_multiple), int(num_permuted_tokens or 0),
+        _ptr(ids) if (rmap is not None and T > 0) else None,
+        _ptr(probs) if (rmap is not None and T > 0) else None, L.ref, _stream(stream))
+    _check(rc, "ep_dispatch_layout_routed")
+    return L, ids, probs
+
+
+def routing_map_to_topk(routing_map: torch.Tensor, dense_probs: torch.Tensor | None, K: int,
+                        out=None, stream=None):
+    """ep_routing_map_to_topk -> (topk_ids int32 [T, K], topk_probs fp32 [T, K] or None)."""
+    if routing_map.dtype not in (torch.uint8, torch.bool) or routing_map.dim() != 2:
+        raise TypeError("routing_map must be a uint8 / bool [T, E] tensor")
+    T, E = routing_map.shape
+    if dense_probs is not None:
+        _need(dense_probs, None, E, (torch.float32,), "dense_probs", exact_rows=T)
+    if out is None:
+        out = (torch.empty(max(T, 1), K, dtype=torch.int32, device=routing_map.device),
+               torch.empty(max(T, 1), K, dtype=torch.float32, device=routing_map.device)
+               if dense_probs is not None else None)
+    ids, probs = out
+    _need(ids, T, K, (torch.int32,), "topk_ids")
+    if probs is not None:
+        _need(probs, T, K, (torch.float32,), "topk_probs")
+    rmap = routing_map.view(torch.uint8) if routing_map.dtype == torch.bool else routing_map
+    rc = _lib.ep_routing_map_to_topk(_ptr(rmap), _ptr(dense_probs), T, E, K, _ptr(ids), _ptr(probs),
+                                     _stream(stream))
+    _check(rc, "ep_routing_map_to_topk")
+    return ids, probs
+
+
+def indices_to_multihot(topk_ids: torch.Tensor, topk_probs: torch.Tensor | None, n_experts: int,
+                        out=None, stream=None):
+    """ep_indices_to_multihot -> (routing_map uint8 [T, E], dense_probs fp32 [T, E] or None)."""
+    if topk_ids.dtype != torch.int32 or topk_ids.dim() != 2:
+        raise TypeError("topk_ids must be an int32 [T, K] tensor")
+    T, K = topk_ids.shape
+    if topk_probs is not None:
+        _need(topk_probs, None, K, (torch.float32,), "topk_probs", exact_rows=T)
+    if out is None:
+        out = (torch.empty(max(T, 1), n_experts, dtype=torch.uint8, device=topk_ids.device),
+               torch.empty(max(T, 1), n_experts, dtype=torch.float32, device=topk_ids.device)
+               if topk_probs is not None else None)
+    rmap, dense = out
+    _need(rmap, T, n_experts, (torch.uint8,), "routing_map")
+    if dense is not None:
+        _need(dense, T, n_experts, (torch.float32,), "dense_probs")
+    rc = _lib.ep_indices_to_multihot(_ptr(topk_ids), _ptr(topk_probs), T, K, n_experts, _ptr(rmap),
+                                     _ptr(dense), _stream(stream))
+    _check(rc, "ep_indices_to_multihot")
+    return rmap, dense
+
+
+def dispatch_fp8(x: torch.Tensor, L: Layout, out=None, stream=None):
+    """ep_dispatch_fp8 -> (E4M3 codes uint8 [R_max, H], fp32 scales [R_max, H/128])."""
+    T, H = x.shape
+    _need(x, None, H, _BF16, "input_tokens", exact_rows=L.T)
+    if H % 128:
+        raise ValueError("FP8 dispatch needs H % 128 == 0")
+    if out is None:
+        out = (torch.empty(max(L.R_max, 1), H, dtype=torch.uint8, device=x.device),
+               torch.empty(max(L.R_max, 1), H // 128, dtype=torch.float32, device=x.device))
+    codes, sc = out
+    _need(codes, L.R_max, H, (torch.uint8,), "out_fp8")
+    _need(sc, L.R_max, H // 128, (torch.float32,), "out_scales")
+    rc = _lib.ep_dispatch_fp8(_bits(x), H, L.ref, _ptr(codes), _ptr(sc), _stream(stream))
+    _check(rc, "ep_dispatch_fp8")
     return out
 
 
@@ -271,9 +415,8 @@ def dispatch_layout_nvfp4(topk_ids: torch.Tensor, x: torch.Tensor, n_experts: in
         raise ValueError("x and topk_ids disagree on the number of tokens")
     S = int(bool(fused_shared))
     L = out_layout
-    if L is not None and (L.T, L.K, L.E, L.P, L.S) != (T, K, n_experts, n_parts, S):
-        raise ValueError("layout buffers were allocated for other sizes "
-                         f"{(L.T, L.K, L.E, L.P, L.S)}")
+    if L is not None and L.shape_key() != (T, K, n_experts, n_parts, S, 1, 0):
+        raise ValueError(f"layout buffers were allocated for other sizes {L.shape_key()}")
     if L is None:
         L = Layout(T, K, n_experts, n_parts, fused_shared, topk_ids.device)
     _need(x, None, H, _BF16, "input_tokens", exact_rows=T)

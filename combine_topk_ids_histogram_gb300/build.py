@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libep_gb300.so")
 
-SOURCES = ["ep_layout.cu", "ep_dispatch.cu", "ep_combine.cu"]
+SOURCES = ["ep_layout.cu", "ep_dispatch.cu", "ep_combine.cu", "ep_routing.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

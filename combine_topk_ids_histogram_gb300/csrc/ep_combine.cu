@@ -193,7 +193,7 @@ template <bool WEIGHTED>
 int launch_combine(const uint16_t *y, const float *probs, int H, const ep_layout_t *L,
                    uint16_t *out, cudaStream_t st) {
     const int K = L->K;
-    const int R_max = (int)rows_max(L->T, L->K, L->fused_shared);
+    const int R_max = layout_rows(L);
     if (K <= 2) return launch_combine_k<2, WEIGHTED>(y, probs, H, L, R_max, out, st);
     if (K <= 4) return launch_combine_k<4, WEIGHTED>(y, probs, H, L, R_max, out, st);
     if (K <= 8) return launch_combine_k<8, WEIGHTED>(y, probs, H, L, R_max, out, st);
@@ -239,19 +239,25 @@ extern "C" int ep_combine_bwd(const uint16_t *grad_out, const uint16_t *expert_o
     const void *ptrs[] = {grad_out, expert_out, probs, grad_expert_out, grad_probs};
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return EP_ERR_INVALID_ARG;
-    if (L->T == 0) return EP_OK;
     cudaStream_t st = as_stream(stream);
-    const int K = L->K;
-    const int R_max = (int)rows_max(L->T, L->K, L->fused_shared);
+    if (L->T > 0) {
+        const int K = L->K;
+        const int R_max = layout_rows(L);
+        int rc;
 #define EP_BWD_CASE(KM)                                                                        \
-    return launch_pdl(ep_combine_bwd_kernel<KM>, dim3(L->T), dim3(kCombineThreads), 0, st,     \
-                      grad_out, expert_out, probs, L->T, H, K, L->E, L->fused_shared, R_max,   \
-                      (const int32_t *)L->row_of, (const int32_t *)L->row_offsets,             \
-                      (const int32_t *)L->status, grad_expert_out, grad_probs)
-    if (K <= 2) EP_BWD_CASE(2);
-    if (K <= 4) EP_BWD_CASE(4);
-    if (K <= 8) EP_BWD_CASE(8);
-    if (K <= 16) EP_BWD_CASE(16);
-    EP_BWD_CASE(32);
+    rc = launch_pdl(ep_combine_bwd_kernel<KM>, dim3(L->T), dim3(kCombineThreads), 0, st,       \
+                    grad_out, expert_out, probs, L->T, H, K, L->E, L->fused_shared, R_max,     \
+                    (const int32_t *)L->row_of, (const int32_t *)L->row_offsets,               \
+                    (const int32_t *)L->status, grad_expert_out, grad_probs)
+        if (K <= 2) EP_BWD_CASE(2);
+        else if (K <= 4) EP_BWD_CASE(4);
+        else if (K <= 8) EP_BWD_CASE(8);
+        else if (K <= 16) EP_BWD_CASE(16);
+        else EP_BWD_CASE(32);
 #undef EP_BWD_CASE
+        if (rc != EP_OK) return rc;
+    }
+    // a padding row's gradient is zero
+    return launch_fill_padding(L, PadFill{grad_expert_out, 2 * H, 0u}, PadFill{nullptr, 0, 0u},
+                               PadFill{nullptr, 0, 0u}, st);
 }

@@ -1,6 +1,8 @@
 // ep_dispatch.cu -- permute-scatter of token rows into the expert-major layout, as NVFP4 with
 // a per-token global scale (Mojo EP dispatch page, DistributedEPDispatchBlockScaledNVDynGlobal
-// Scales.execute) or as plain bf16 (fused_a2a page, HybridEPDispatch.forward).
+// Scales.execute), as plain bf16 (fused_a2a page, HybridEPDispatch.forward) or as FP8 with
+// per-block scales (fused_a2a page, init_hybrid_ep_buffer, fp8_dispatch); and the padding rows
+// of padded layouts (token_dispatcher page, TokenDispatcherConfig.moe_router_expert_pad_multiple).
 //
 // NVFP4 kernel: one CTA per token.  Each thread owns a contiguous chunk of BPT 16-element
 // blocks (BPT = 2 -> 32 elements: 4 x 16-byte loads in, one 16-byte code store and one 2-byte
@@ -169,6 +171,122 @@ ep_dispatch_bf16_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int
 }
 
 // ---------------------------------------------------------------------------------------
+// FP8 dispatch: one CTA per token, one thread per 32 elements, so the four threads of a
+// 128-element block share its maximum through two shuffles.  Per block, in fp32 with every
+// operation rounded once: s = 448 / max|x| (1 for an all-zero block, FLT_MAX if it overflows),
+// code = E4M3(x * s) by the hardware conversion, scale = 1 / s.  The row is read once and its
+// 32 code bytes per thread are stored to each of the token's K (+1 shared) rows.
+// ---------------------------------------------------------------------------------------
+constexpr int kFp8Block = 128;
+
+template <int MAXT, int MINB>
+__global__ void __launch_bounds__(MAXT, MINB)
+ep_dispatch_fp8_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int E, int S, int R_max,
+                       const int32_t *__restrict__ row_of, const int32_t *__restrict__ row_offsets,
+                       const int32_t *__restrict__ status, uint8_t *__restrict__ out_fp8,
+                       float *__restrict__ out_scales) {
+    __shared__ int s_rows[kMaxRowsPerToken];
+    pdl_begin();
+    const int tid = threadIdx.x;
+    const int t = blockIdx.x;
+    const bool active = tid < H / 32;
+    uint4 v[4];
+    if (active) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H) + (size_t)tid * 4;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = ld_stream(src + i);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = make_uint4(0, 0, 0, 0);
+    }
+    int my_row = -1;
+    if (tid < K) my_row = row_of[(size_t)t * K + tid];
+    else if (tid == K && S) my_row = row_offsets[E] + t;
+    if (load_status(status)) return;
+    if (tid < K + S) s_rows[tid] = my_row;
+    float m = fmaxf(fmaxf(absmax8(v[0]), absmax8(v[1])), fmaxf(absmax8(v[2]), absmax8(v[3])));
+    m = fmaxf(m, __shfl_xor_sync(kFullMask, m, 1));   // the four threads of the block
+    m = fmaxf(m, __shfl_xor_sync(kFullMask, m, 2));
+    __syncthreads();
+    if (!active) return;
+    float sc = 1.0f;
+    if (m != 0.0f) {
+        sc = __fdiv_rn(448.0f, m);
+        if (isinf(sc)) sc = FLT_MAX;
+    }
+    const float scale = __frcp_rn(sc);
+    const uint32_t w[16] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w,
+                            v[2].x, v[2].y, v[2].z, v[2].w, v[3].x, v[3].y, v[3].z, v[3].w};
+    uint32_t c[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const uint32_t lo = cvt_e4m3x2(__fmul_rn(bf16_lo(w[2 * q]), sc), __fmul_rn(bf16_hi(w[2 * q]), sc));
+        const uint32_t hi =
+            cvt_e4m3x2(__fmul_rn(bf16_lo(w[2 * q + 1]), sc), __fmul_rn(bf16_hi(w[2 * q + 1]), sc));
+        c[q] = lo | (hi << 16);
+    }
+    const int nrows = K + S;
+    const int nblk = H / kFp8Block;
+    for (int k = 0; k < nrows; ++k) {
+        const int r = s_rows[k];
+        if (r < 0 || r >= R_max) continue;
+        uint8_t *dst = out_fp8 + (size_t)r * H + (size_t)tid * 32;
+        st_stream(dst, make_uint4(c[0], c[1], c[2], c[3]));
+        st_stream(dst + 16, make_uint4(c[4], c[5], c[6], c[7]));
+        if ((tid & 3) == 0) __stcs(out_scales + (size_t)r * nblk + (tid >> 2), scale);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Padding rows of a padded layout: every row below min(row_offsets[G], R_max) whose source
+// token is -1 receives the bytes an all-zero token dispatches to (up to three buffers).  Each
+// CTA takes kFillRows rows at a time: one thread per row tests it, the padding rows are listed
+// in shared memory, and one warp writes each listed row.
+// ---------------------------------------------------------------------------------------
+constexpr int kFillRows = 256;
+
+__device__ __forceinline__ void fill_row(const PadFill &f, int row, int lane) {
+    if (!f.ptr) return;
+    unsigned char *p = static_cast<unsigned char *>(f.ptr) + (size_t)row * f.row_bytes;
+    if (f.row_bytes % 16 == 0) {
+        const uint4 v = make_uint4(f.pattern, f.pattern, f.pattern, f.pattern);
+        for (int i = lane; i < f.row_bytes / 16; i += 32) reinterpret_cast<uint4 *>(p)[i] = v;
+    } else if (f.row_bytes % 4 == 0) {
+        for (int i = lane; i < f.row_bytes / 4; i += 32) reinterpret_cast<uint32_t *>(p)[i] = f.pattern;
+    } else {
+        for (int i = lane; i < f.row_bytes / 2; i += 32)
+            reinterpret_cast<uint16_t *>(p)[i] = (uint16_t)f.pattern;
+    }
+}
+
+__global__ void __launch_bounds__(kFillRows)
+ep_fill_padding_kernel(const int32_t *__restrict__ src_info, const int32_t *__restrict__ row_offsets,
+                       int G, int R_max, const int32_t *__restrict__ status, PadFill f0, PadFill f1,
+                       PadFill f2) {
+    __shared__ int s_list[kFillRows];
+    __shared__ int s_n;
+    pdl_begin();
+    if (load_status(status)) return;
+    const int end = min(row_offsets[G], R_max);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int base = blockIdx.x * kFillRows; base < end; base += gridDim.x * kFillRows) {
+        if (tid == 0) s_n = 0;
+        __syncthreads();
+        const int r = base + tid;
+        if (r < end && src_info[2 * (size_t)r] < 0) s_list[atomicAdd(&s_n, 1)] = r;
+        __syncthreads();
+        const int n = s_n;
+        for (int i = warp; i < n; i += kFillRows / 32) {
+            const int row = s_list[i];
+            fill_row(f0, row, lane);
+            fill_row(f1, row, lane);
+            fill_row(f2, row, lane);
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------------------
 // Staged NVFP4 dispatch (H % 256 == 0, H <= 8192): as many CTAs as fit on the GPU (several per
 // SM), each owning a contiguous range of tokens, with the per-token kernel's thread layout (one
 // thread per 32 elements).  In rounds of up to kStageSlots tokens:
@@ -311,7 +429,7 @@ inline int launch_nvfp4_staged(const uint16_t *x, int H, const ep_layout_t *L, u
     const int tpc = (T + grid - 1) / grid;
     grid = (T + tpc - 1) / tpc;
     const int G = L->E + L->fused_shared;
-    const int R_max = (int)rows_max(L->T, L->K, L->fused_shared);
+    const int R_max = layout_rows(L);
     return launch_pdl(ep_dispatch_nvfp4_staged_kernel, dim3(grid), dim3(threads), smem, st, x, T, H,
                       L->K, L->E, L->fused_shared, G, R_max, tpc, early, (const int32_t *)L->row_of,
                       (const int32_t *)L->row_offsets, (const int32_t *)L->status, out_fp4, out_scales,
@@ -359,7 +477,7 @@ int launch_nvfp4(const uint16_t *input_tokens, int H, const ep_layout_t *L, uint
     const int threads = max((nth + 31) / 32 * 32, (L->K + 1 + 31) / 32 * 32);
     const int grid = L->T > 0 ? L->T : 1;
     const int G = L->E + L->fused_shared;
-    const int R_max = (int)rows_max(L->T, L->K, L->fused_shared);
+    const int R_max = layout_rows(L);
     const int32_t *row_of = L->row_of, *row_offsets = L->row_offsets, *status = L->status;
 #define EP_NVFP4_LAUNCH(BPT, MAXT, MINB)                                                        \
     return launch_pdl(ep_dispatch_nvfp4_kernel<BPT, MAXT, MINB>, dim3(grid), dim3(threads), 0, st, \
@@ -375,13 +493,32 @@ int launch_nvfp4(const uint16_t *input_tokens, int H, const ep_layout_t *L, uint
 }
 
 }  // namespace
+
+int launch_fill_padding(const ep_layout_t *L, PadFill a, PadFill b, PadFill c, cudaStream_t st) {
+    if (!layout_padded(L)) return EP_OK;
+    const int R_max = layout_rows(L);
+    if (R_max == 0) return EP_OK;
+    int grid = (R_max + kFillRows - 1) / kFillRows;
+    const int cap = resident_blocks(ep_fill_padding_kernel, kFillRows, 0);
+    if (cap > 0 && grid > cap) grid = cap;
+    return launch_pdl(ep_fill_padding_kernel, dim3(grid), dim3(kFillRows), 0, st,
+                      (const int32_t *)L->src_info, (const int32_t *)L->row_offsets,
+                      L->E + L->fused_shared, R_max, (const int32_t *)L->status, a, b, c);
+}
+
 }  // namespace ep
 
 extern "C" int ep_dispatch_nvfp4(const uint16_t *input_tokens, int hidden_size, const ep_layout_t *L,
                                  uint8_t *out_fp4, uint8_t *out_scales, uint16_t *out_rowwise_inv_scale,
                                  int32_t *scales_offsets, void *stream) {
-    return launch_nvfp4(input_tokens, hidden_size, L, out_fp4, out_scales, out_rowwise_inv_scale,
-                        scales_offsets, 0, as_stream(stream));
+    cudaStream_t st = as_stream(stream);
+    const int rc = launch_nvfp4(input_tokens, hidden_size, L, out_fp4, out_scales,
+                                out_rowwise_inv_scale, scales_offsets, 0, st);
+    if (rc != EP_OK) return rc;
+    // padding rows: codes 0, block scales 0, inverse global scale bf16(1/1) = 0x3F80
+    const int H = hidden_size;
+    return launch_fill_padding(L, PadFill{out_fp4, H / 2, 0u}, PadFill{out_scales, H / 16, 0u},
+                               PadFill{out_rowwise_inv_scale, 2, 0x3F803F80u}, st);
 }
 
 extern "C" int ep_dispatch_layout_nvfp4(const int32_t *topk_ids, int T, int K, int n_experts,
@@ -400,7 +537,8 @@ extern "C" int ep_dispatch_layout_nvfp4(const int32_t *topk_ids, int T, int K, i
         if (p && !aligned16(p)) return EP_ERR_INVALID_ARG;
     cudaStream_t st = as_stream(stream);
     int layout_sms = 0;
-    int rc = launch_layout(topk_ids, T, K, n_experts, n_parts, capacity, fused_shared, L, st, &layout_sms);
+    int rc = launch_layout(topk_ids, T, K, n_experts, n_parts, capacity, fused_shared, 1, 0, L, st,
+                           &layout_sms);
     if (rc != EP_OK) return rc;
     // The dispatch kernel directly follows the layout kernel, which lets it launch only once
     // every earlier kernel of the stream has completed, so its CTAs read and quantise their
@@ -418,11 +556,47 @@ extern "C" int ep_dispatch_bf16(const uint16_t *input_tokens, int hidden_size, c
     if (!layout_ok(L) || !hidden_ok(H)) return EP_ERR_INVALID_ARG;
     if (L->T > 0 && (!input_tokens || !out)) return EP_ERR_INVALID_ARG;
     if ((input_tokens && !aligned16(input_tokens)) || (out && !aligned16(out))) return EP_ERR_INVALID_ARG;
-    if (L->T == 0) return EP_OK;
-    return launch_pdl(ep_dispatch_bf16_kernel, dim3(L->T), dim3(256), 0, as_stream(stream),
-                      input_tokens, L->T, H, L->K, L->E, L->fused_shared,
-                      (int)rows_max(L->T, L->K, L->fused_shared), (const int32_t *)L->row_of,
-                      (const int32_t *)L->row_offsets, (const int32_t *)L->status, out);
+    cudaStream_t st = as_stream(stream);
+    if (L->T > 0) {
+        const int rc = launch_pdl(ep_dispatch_bf16_kernel, dim3(L->T), dim3(256), 0, st, input_tokens,
+                                  L->T, H, L->K, L->E, L->fused_shared, layout_rows(L),
+                                  (const int32_t *)L->row_of, (const int32_t *)L->row_offsets,
+                                  (const int32_t *)L->status, out);
+        if (rc != EP_OK) return rc;
+    }
+    return launch_fill_padding(L, PadFill{out, 2 * H, 0u}, PadFill{nullptr, 0, 0u},
+                               PadFill{nullptr, 0, 0u}, st);
+}
+
+extern "C" int ep_dispatch_fp8(const uint16_t *input_tokens, int hidden_size, const ep_layout_t *L,
+                               uint8_t *out_fp8, float *out_scales, void *stream) {
+    const int H = hidden_size;
+    if (!layout_ok(L) || !hidden_ok(H) || H % kFp8Block != 0) return EP_ERR_INVALID_ARG;
+    if (L->T > 0 && (!input_tokens || !out_fp8 || !out_scales)) return EP_ERR_INVALID_ARG;
+    const void *ptrs[] = {input_tokens, out_fp8, out_scales};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return EP_ERR_INVALID_ARG;
+    cudaStream_t st = as_stream(stream);
+    if (L->T > 0) {
+        const int threads = max(H / 32, 32 * ((L->K + 1 + 31) / 32));   // H % 128 == 0: whole warps
+        const int R_max = layout_rows(L);
+        int rc;
+        if (threads <= 256)
+            rc = launch_pdl(ep_dispatch_fp8_kernel<256, 5>, dim3(L->T), dim3(threads), 0, st,
+                            input_tokens, L->T, H, L->K, L->E, L->fused_shared, R_max,
+                            (const int32_t *)L->row_of, (const int32_t *)L->row_offsets,
+                            (const int32_t *)L->status, out_fp8, out_scales);
+        else
+            rc = launch_pdl(ep_dispatch_fp8_kernel<1024, 1>, dim3(L->T), dim3(threads), 0, st,
+                            input_tokens, L->T, H, L->K, L->E, L->fused_shared, R_max,
+                            (const int32_t *)L->row_of, (const int32_t *)L->row_offsets,
+                            (const int32_t *)L->status, out_fp8, out_scales);
+        if (rc != EP_OK) return rc;
+    }
+    // padding rows: codes 0 and the scale of an all-zero block, 1.0f
+    return launch_fill_padding(L, PadFill{out_fp8, H, 0u},
+                               PadFill{out_scales, 4 * (H / kFp8Block), 0x3F800000u},
+                               PadFill{nullptr, 0, 0u}, st);
 }
 
 extern "C" int ep_cvt_e2m1(const float *in, uint8_t *codes, long n, void *stream) {

@@ -21,8 +21,18 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
+constexpr int kMaxPad = 65536;
+
 // Rows every dispatched buffer holds: T*K routed rows plus one shared row per token.
 inline long long rows_max(int T, int K, int S) { return (long long)T * K + (long long)S * T; }
+
+// Rows every dispatched buffer holds for a padded layout: the static row capacity when one is
+// set, else the routed and shared rows plus at most pad - 1 padding rows per group.
+inline long long rows_max(int T, int K, int E, int S, int pad, int row_capacity) {
+    if (row_capacity > 0) return row_capacity;
+    const long long p = pad > 1 ? pad : 1;
+    return rows_max(T, K, S) + (long long)(E + S) * (p - 1);
+}
 
 inline bool sizes_ok(int T, int K, int E, int S) {
     if (T < 0 || T > kMaxT || K < 1 || K > kMaxK || E < 1 || E > kMaxE) return false;
@@ -30,13 +40,26 @@ inline bool sizes_ok(int T, int K, int E, int S) {
     return rows_max(T, K, S) < (1ll << 31);
 }
 
-// A layout filled by ep_dispatch_layout, with every buffer present.
+// Padding multiple and row capacity of a layout call (pad 1 / capacity 0: none).
+inline bool padding_ok(int T, int K, int E, int S, int pad, int row_capacity) {
+    if (pad < 1 || pad > kMaxPad || row_capacity < 0) return false;
+    return rows_max(T, K, E, S, pad, 0) < (1ll << 31);   // the padded row count fits an int
+}
+
+// A layout filled by a layout call, with every buffer present.
 inline bool layout_ok(const ep_layout_t *L) {
     if (!L || !L->row_offsets || !L->row_of || !L->status) return false;
     if (!sizes_ok(L->T, L->K, L->E, L->fused_shared)) return false;
     if (L->P < 1 || L->P > L->E || L->E % L->P != 0) return false;
-    return true;
+    if (L->pad_multiple < 0 || L->pad_multiple > kMaxPad || L->row_capacity < 0) return false;
+    return rows_max(L->T, L->K, L->E, L->fused_shared, L->pad_multiple, L->row_capacity) < (1ll << 31);
 }
+
+// Rows of every dispatched buffer of a layout, and whether it has padding rows.
+inline int layout_rows(const ep_layout_t *L) {
+    return (int)rows_max(L->T, L->K, L->E, L->fused_shared, L->pad_multiple, L->row_capacity);
+}
+inline bool layout_padded(const ep_layout_t *L) { return L->pad_multiple > 1; }
 
 inline bool hidden_ok(int H) { return H >= 16 && H <= kMaxH && H % 16 == 0; }
 
@@ -101,9 +124,27 @@ inline int resident_blocks(K kernel, int threads, size_t smem) {
     return blocks;
 }
 
-// Enqueues a dispatch layout (ep_layout.cu).  *cluster_ctas_used receives the number of SMs the
-// single-cluster layout kernel occupies, or 0 when the two-kernel path ran.
+// Enqueues a dispatch layout (ep_layout.cu) with groups padded to a multiple of `pad` and at
+// most `row_capacity` rows (0: the default R_max).  *cluster_ctas_used receives the number of
+// SMs the single-cluster layout kernel occupies, or 0 when the two-kernel path ran.
 int launch_layout(const int32_t *topk_ids, int T, int K, int E, int P, int capacity, int S,
-                  ep_layout_t *L, cudaStream_t st, int *cluster_ctas_used);
+                  int pad, int row_capacity, ep_layout_t *L, cudaStream_t st,
+                  int *cluster_ctas_used);
+
+// Enqueues the routing-map -> compact ids conversion (ep_routing.cu); arguments checked.
+int launch_map_to_topk(const uint8_t *routing_map, const float *dense_probs, int T, int E, int K,
+                       int32_t *topk_ids, float *topk_probs, cudaStream_t st);
+
+// One buffer whose padding rows a dispatch fills: `row_bytes` per row (even), every 32-bit
+// word of a padding row set to `pattern` (16-bit periodic when row_bytes % 4 != 0).
+struct PadFill {
+    void *ptr;
+    int row_bytes;
+    uint32_t pattern;
+};
+
+// Enqueues the fill of the padding rows of up to three buffers of a padded layout
+// (ep_dispatch.cu); EP_OK without a launch when the layout has no padding.
+int launch_fill_padding(const ep_layout_t *L, PadFill a, PadFill b, PadFill c, cudaStream_t st);
 
 }  // namespace ep

@@ -141,16 +141,16 @@ __device__ __forceinline__ void count_partition_tokens(const int *s_ids, int nto
 
 // Stable ranks of one warp's run [w0, w1) of a token range's flat (t, k) indices, the range
 // starting at token t0; hist holds the warp's next row per expert and is advanced.  Writes
-// row_of, src_info and expert_ids.  The (token, slot) of each lane's index is carried from
-// chunk to chunk by adding 32 with a carry, so there is one division per lane, not per id.
-__device__ __forceinline__ void rank_and_write(const int *s_ids, int w0, int w1, int t0, int T, int K,
-                                               int nbits, int *hist, int32_t *row_of,
+// row_of, src_info and expert_ids; a row at or past row_limit (the layout's row capacity) is
+// not recorded and its pair gets row_of -1.  The (token, slot) of each lane's index is carried
+// from chunk to chunk by adding 32 with a carry, so there is one division per lane, not per id.
+__device__ __forceinline__ void rank_and_write(const int *s_ids, int w0, int w1, int t0, int K,
+                                               int row_limit, int nbits, int *hist, int32_t *row_of,
                                                int32_t *src_info, int32_t *expert_ids) {
     const int lane = threadIdx.x & 31;
     const unsigned lt_mask = (1u << lane) - 1u;
     int tk = (w0 + lane) / K, kk = (w0 + lane) - tk * K;
     const int step_t = 32 / K, step_k = 32 - step_t * K;
-    const int limit = T * K;
     for (int base = w0; base < w1; base += 32) {
         const int i = base + lane;
         const int id = i < w1 ? s_ids[i] : -1;
@@ -161,7 +161,7 @@ __device__ __forceinline__ void rank_and_write(const int *s_ids, int w0, int w1,
         if (id >= 0 && lane == __ffs(peers) - 1) hist[id] += __popc(peers);
         __syncwarp();
         if (i < w1) {
-            if (row >= limit) row = -1;   // only a layout raced by a concurrent writer of ids
+            if (row >= row_limit) row = -1;
             row_of[(size_t)t0 * K + i] = row;
             if (row >= 0) {
                 reinterpret_cast<int2 *>(src_info)[row] = make_int2(t0 + tk, kk);
@@ -210,7 +210,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int &t
 
 __global__ void __launch_bounds__(kLayoutThreads)
 ep_layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int P, int C, int S,
-                       int tile_t, int nTiles, unsigned long long per_magic, Workspace ws, int32_t *__restrict__ row_offsets,
+                       int pad, int row_limit, int tile_t, int nTiles, unsigned long long per_magic,
+                       Workspace ws, int32_t *__restrict__ row_offsets,
                        int32_t *__restrict__ part_tokens, int32_t *__restrict__ status) {
     extern __shared__ int smem[];
     int *s_hist = smem;          // [E]
@@ -260,6 +261,19 @@ ep_layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int
     __syncthreads();
     if (!s_last) return;
     __threadfence();
+
+    // Padding: each expert's padding rows follow its last tile's rows, so they are added to
+    // that tile's count before the scan (the scan is exclusive: the tile's own base is unchanged).
+    if (pad > 1) {
+        for (int e = tid; e < E; e += blockDim.x) {
+            int tot = 0;
+#pragma unroll 8
+            for (int jj = 0; jj < nTiles; ++jj) tot += __ldcg(ws.cnt + (size_t)e * nTiles + jj);
+            const int extra = (tot + pad - 1) / pad * pad - tot;
+            if (extra) ws.cnt[(size_t)e * nTiles + nTiles - 1] = __ldcg(ws.cnt + (size_t)e * nTiles + nTiles - 1) + extra;
+        }
+        __syncthreads();
+    }
 
     // Exclusive scan of cnt in place, kScanChunk entries per pass, through shared memory
     // (padded by one word per 32 so each thread's contiguous segment is conflict-free).  All
@@ -312,9 +326,10 @@ ep_layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int
         carry += tot;
         __syncthreads();
     }
+    const long long rows_needed = (long long)carry + (S ? (long long)(T + pad - 1) / pad * pad : 0);
     if (tid == 0) {
         row_offsets[E] = carry;
-        if (S) row_offsets[E + 1] = carry + T;
+        if (S) row_offsets[E + 1] = (int)rows_needed;
     }
     // Partition totals against the capacity (one warp per partition, lanes over the tiles),
     // and the bad-id flags.
@@ -331,6 +346,7 @@ ep_layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int
     }
     for (int jj = tid; jj < nTiles; jj += blockDim.x)
         if (__ldcg(ws.tile_flags + jj)) flags |= EP_STATUS_BAD_EXPERT;
+    if (rows_needed > row_limit) flags |= EP_STATUS_OVERFLOW;   // the row capacity
     flags = __reduce_or_sync(kFullMask, flags);
     if (lane == 0) s_warp[tid >> 5] = flags;
     __syncthreads();
@@ -343,8 +359,8 @@ ep_layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int
 }
 
 __global__ void __launch_bounds__(kLayoutThreads)
-ep_layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int S, int tile_t,
-                      int nTiles, int nbits, const int32_t *__restrict__ cnt,
+ep_layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int S, int pad,
+                      int row_limit, int tile_t, int nTiles, int nbits, const int32_t *__restrict__ cnt,
                       const int32_t *__restrict__ row_offsets, int32_t *__restrict__ row_of,
                       int32_t *__restrict__ src_info, int32_t *__restrict__ expert_ids) {
     extern __shared__ int smem[];
@@ -383,6 +399,9 @@ ep_layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int 
     }
     __syncthreads();
     // First row of each (warp, expert): the tile's scanned base plus earlier warps' counts.
+    // The last tile also writes each expert's padding rows: from the end of its routed rows
+    // to the next group's first row.
+    const bool last_tile = j == nTiles - 1;
 #pragma unroll
     for (int q = 0; q < kMaxEPerThread; ++q) {
         const int e = tid + q * kLayoutThreads;
@@ -393,14 +412,28 @@ ep_layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int 
             s_whist[w * E + e] = run;
             run += c;
         }
+        if (pad > 1 && last_tile) {
+            const int end = min(row_offsets[e + 1], row_limit);
+            for (int r = run; r < end; ++r) {
+                reinterpret_cast<int2 *>(src_info)[r] = make_int2(-1, -1);
+                expert_ids[r] = e;
+            }
+        }
     }
     __syncthreads();
-    rank_and_write(s_ids, w0, w1, t0, T, K, nbits, hist, row_of, src_info, expert_ids);
+    rank_and_write(s_ids, w0, w1, t0, K, row_limit, nbits, hist, row_of, src_info, expert_ids);
     if (S) {
         const int rs = row_offsets[E];
-        for (int t = t0 + tid; t < t1; t += blockDim.x) {
+        for (int t = t0 + tid; t < t1 && rs + t < row_limit; t += blockDim.x) {
             reinterpret_cast<int2 *>(src_info)[rs + t] = make_int2(t, K);
             expert_ids[rs + t] = E;
+        }
+        if (pad > 1 && last_tile) {
+            const int end = min(row_offsets[E + 1], row_limit);
+            for (int r = rs + T + tid; r < end; r += blockDim.x) {
+                reinterpret_cast<int2 *>(src_info)[r] = make_int2(-1, -1);
+                expert_ids[r] = E;
+            }
         }
     }
 }
@@ -481,7 +514,7 @@ __device__ __forceinline__ void cluster_sync_all() {
 
 __global__ void __launch_bounds__(kClThreads, 1)
 ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int P, int C, int S,
-                         int tile_t, int nbits, unsigned long long per_magic,
+                         int pad, int row_limit, int tile_t, int nbits, unsigned long long per_magic,
                          unsigned long long k_magic, int32_t *__restrict__ row_offsets,
                          int32_t *__restrict__ expert_ids, int32_t *__restrict__ src_info,
                          int32_t *__restrict__ row_of, int32_t *__restrict__ part_tokens,
@@ -602,7 +635,8 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
     if (tid == 0) cluster.map_shared_rank(s_bad_all, 0)[crank] = s_bad;
     cluster_sync_all();
 
-    //    cluster totals per expert (thread tid owns experts kClExpertsPerThread*tid + q)
+    //    cluster totals per expert (thread tid owns experts kClExpertsPerThread*tid + q), and
+    //    their extents: the totals rounded up to a multiple of pad
     int mine = 0, mine_local = 0;
     int before[kClExpertsPerThread], total[kClExpertsPerThread];
 #pragma unroll
@@ -621,7 +655,7 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
             }
             mine_local += s_hist[e];
         }
-        mine += total[q];
+        mine += pad > 1 ? (total[q] + pad - 1) / pad * pad : total[q];
     }
     //    CTA 0: partition totals against the capacity, and the bad-id flags (status bits kept
     //    above bit 4 of s_bad, whose low bit is this CTA's own bad-id flag)
@@ -674,32 +708,40 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
     }
     __syncthreads();
     const int routed = s_routed, n_valid = s_nvalid;
-    const int flags = crank == 0 ? (s_bad >> 4) : 0;
+    const int shared_ext = S ? (pad > 1 ? (T + pad - 1) / pad * pad : T) : 0;
     int excl = s_warp[warp] + incl - mine;
     int excl_l = s_warp2[warp] + incl_l - mine_local;
 #pragma unroll
     for (int q = 0; q < kClExpertsPerThread; ++q) {
         const int e = kClExpertsPerThread * tid + q;
+        const int ext = pad > 1 ? (total[q] + pad - 1) / pad * pad : total[q];
         if (e < E) {
             if (crank == 0) row_offsets[e] = excl;
             s_first[e] = excl + before[q];
             s_locoff[e] = excl_l;
             excl_l += s_hist[e];
+            // padding rows of expert e, spread over the cluster's CTAs
+            for (int r = excl + total[q] + crank; r < excl + ext && r < row_limit; r += ncta) {
+                reinterpret_cast<int2 *>(src_info)[r] = make_int2(-1, -1);
+                expert_ids[r] = e;
+            }
         }
-        excl += total[q];
+        excl += ext;
     }
     if (crank == 0 && tid == 0) {
+        int flags = s_bad >> 4;
+        if ((long long)routed + shared_ext > row_limit) flags |= EP_STATUS_OVERFLOW;   // row capacity
         row_offsets[E] = routed;
-        if (S) row_offsets[E + 1] = routed + T;
+        if (S) row_offsets[E + 1] = routed + shared_ext;
         *status = flags;
     }
     __syncthreads();
 
-    // D. stable ranks: row_of in flat order; each routed (t, k) staged at its expert-ordered
-    //    local position (flat index in the low bits, expert in the high bits).
+    // D. stable ranks: row_of in flat order (-1 for a row at or past the row capacity); each
+    //    routed (t, k) staged at its expert-ordered local position (flat index in the low bits,
+    //    expert in the high bits).
     {
         const unsigned lt_mask = (1u << lane) - 1u;
-        const int limit = T * K;
         for (int base = w0; base < w1; base += 32) {
             const int i = base + lane;
             const int id = i < w1 ? s_ids[i] : -1;
@@ -713,8 +755,8 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
                 int row = -1;
                 if (id >= 0) {
                     row = s_first[id] + local;
-                    if (row >= limit) row = -1;
-                    else s_stage[s_locoff[id] + local] = (id << 16) | i;
+                    if (row >= row_limit) row = -1;
+                    s_stage[s_locoff[id] + local] = (id << 16) | i;
                 }
                 row_of[(size_t)t0 * K + i] = row;
             }
@@ -726,15 +768,21 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
         const int e = v >> 16, i = v & 0xffff;
         if (e < 0 || e >= E || i >= n) continue;   // only a layout raced by a writer of ids
         const int row = s_first[e] + (j - s_locoff[e]);
-        if (row < 0 || row >= T * K) continue;
+        if (row < 0 || row >= row_limit) continue;
         const int tk = div_magic((unsigned)i, k_magic);
         reinterpret_cast<int2 *>(src_info)[row] = make_int2(t0 + tk, i - tk * K);
         expert_ids[row] = e;
     }
     if (S) {
-        for (int t = t0 + tid; t < t1; t += kClThreads) {
+        for (int t = t0 + tid; t < t1 && routed + t < row_limit; t += kClThreads) {
             reinterpret_cast<int2 *>(src_info)[routed + t] = make_int2(t, K);
             expert_ids[routed + t] = E;
+        }
+        // the shared group's padding rows, spread over the cluster's CTAs
+        const int end = min(routed + shared_ext, row_limit);
+        for (int r = routed + T + crank * kClThreads + tid; r < end; r += ncta * kClThreads) {
+            reinterpret_cast<int2 *>(src_info)[r] = make_int2(-1, -1);
+            expert_ids[r] = E;
         }
     }
 }
@@ -775,7 +823,8 @@ inline int max_cluster_ctas() {
 // The whole layout as one cluster of CTAs (see ep_layout_cluster_kernel).  Returns -1 when the
 // sizes do not fit one cluster (the caller then uses the two-kernel path).
 inline int launch_cluster_layout(const int32_t *ids, int T, int K, int E, int P, int C, int S,
-                                 ep_layout_t *L, cudaStream_t st, int *ctas_used) {
+                                 int pad, int row_limit, ep_layout_t *L, cudaStream_t st,
+                                 int *ctas_used) {
     const int ncta = cluster_ctas(T, K, E, P, max_cluster_ctas());
     if (ncta == 0) return -1;
     *ctas_used = ncta;
@@ -801,7 +850,8 @@ inline int launch_cluster_layout(const int32_t *ids, int T, int K, int E, int P,
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     return launch_result(cudaLaunchKernelEx(&cfg, ep_layout_cluster_kernel, ids, T, K, E, P, C, S,
-                                            tile_t, key_bits(E + 1), magic_of(E / P), magic_of(K),
+                                            pad, row_limit, tile_t, key_bits(E + 1), magic_of(E / P),
+                                            magic_of(K),
                                             L->row_offsets, L->expert_ids, L->src_info, L->row_of,
                                             L->part_tokens, L->status));
 }
@@ -822,9 +872,11 @@ namespace ep {
 // Validates the arguments of a layout call and enqueues it.  *cluster_ctas_used receives the
 // number of SMs the single-cluster kernel occupies (0 when the two-kernel path ran).
 int launch_layout(const int32_t *topk_ids, int T, int K, int E, int P, int capacity, int S,
-                  ep_layout_t *L, cudaStream_t st, int *cluster_ctas_used) {
+                  int pad, int row_capacity, ep_layout_t *L, cudaStream_t st,
+                  int *cluster_ctas_used) {
     if (cluster_ctas_used) *cluster_ctas_used = 0;
-    if (!L || !sizes_ok(T, K, E, S)) return EP_ERR_INVALID_ARG;
+    if (!L || !sizes_ok(T, K, E, S) || !padding_ok(T, K, E, S, pad, row_capacity))
+        return EP_ERR_INVALID_ARG;
     if (P < 1 || P > E || E % P != 0 || capacity < 0) return EP_ERR_INVALID_ARG;
     if ((T > 0 && !topk_ids) || !L->row_offsets || !L->expert_ids || !L->src_info ||
         !L->row_of || !L->part_tokens || !L->status || !L->workspace)
@@ -843,9 +895,13 @@ int launch_layout(const int32_t *topk_ids, int T, int K, int E, int P, int capac
     L->P = P;
     L->capacity = capacity;
     L->fused_shared = S;
+    L->pad_multiple = pad;
+    L->row_capacity = row_capacity;
+    const int row_limit = layout_rows(L);
 
     int used = 0;
-    const int rc_cl = launch_cluster_layout(topk_ids, T, K, E, P, capacity, S, L, st, &used);
+    const int rc_cl = launch_cluster_layout(topk_ids, T, K, E, P, capacity, S, pad, row_limit, L,
+                                            st, &used);
     if (rc_cl != -1) {
         if (cluster_ctas_used) *cluster_ctas_used = used;
         return rc_cl;
@@ -853,8 +909,8 @@ int launch_layout(const int32_t *topk_ids, int T, int K, int E, int P, int capac
     Workspace ws = carve(L->workspace, nTiles, E);
     const size_t smem_count = count_smem_bytes(E, P, tt, K);
     int rc = launch_pdl(ep_layout_count_kernel, dim3(nTiles), dim3(kLayoutThreads), smem_count, st,
-                        topk_ids, T, K, E, P, capacity, S, tt, nTiles, magic_of(E / P), ws,
-                        L->row_offsets, L->part_tokens, L->status);
+                        topk_ids, T, K, E, P, capacity, S, pad, row_limit, tt, nTiles,
+                        magic_of(E / P), ws, L->row_offsets, L->part_tokens, L->status);
     if (rc != EP_OK) return rc;
     size_t smem_rank = sizeof(int) * ((size_t)kLayoutWarps * E + (size_t)tt * K);
     if (smem_rank > 48 * 1024 &&
@@ -862,8 +918,9 @@ int launch_layout(const int32_t *topk_ids, int T, int K, int E, int P, int capac
                              (int)smem_rank) != cudaSuccess)
         return EP_ERR_CUDA;
     return launch_pdl(ep_layout_rank_kernel, dim3(nTiles), dim3(kLayoutThreads), smem_rank, st,
-                      topk_ids, T, K, E, S, tt, nTiles, key_bits(E + 1), (const int32_t *)ws.cnt,
-                      (const int32_t *)L->row_offsets, L->row_of, L->src_info, L->expert_ids);
+                      topk_ids, T, K, E, S, pad, row_limit, tt, nTiles, key_bits(E + 1),
+                      (const int32_t *)ws.cnt, (const int32_t *)L->row_offsets, L->row_of,
+                      L->src_info, L->expert_ids);
 }
 
 }  // namespace ep
@@ -871,8 +928,37 @@ int launch_layout(const int32_t *topk_ids, int T, int K, int E, int P, int capac
 extern "C" int ep_dispatch_layout(const int32_t *topk_ids, int T, int K, int n_experts,
                                   int n_parts, int capacity, int fused_shared, ep_layout_t *L,
                                   void *stream) {
-    return launch_layout(topk_ids, T, K, n_experts, n_parts, capacity, fused_shared, L,
+    return launch_layout(topk_ids, T, K, n_experts, n_parts, capacity, fused_shared, 1, 0, L,
                          as_stream(stream), nullptr);
+}
+
+extern "C" size_t ep_rows_max(int T, int K, int n_experts, int fused_shared, int pad_multiple,
+                              int num_permuted_tokens) {
+    if (!sizes_ok(T, K, n_experts, fused_shared) || num_permuted_tokens < 0) return 0;
+    const int pad = pad_multiple < 1 ? 1 : pad_multiple;
+    if (!padding_ok(T, K, n_experts, fused_shared, pad, num_permuted_tokens)) return 0;
+    return (size_t)rows_max(T, K, n_experts, fused_shared, pad, num_permuted_tokens);
+}
+
+extern "C" int ep_dispatch_layout_routed(const int32_t *topk_ids, const uint8_t *routing_map,
+                                         const float *dense_probs, int T, int K, int n_experts,
+                                         int n_parts, int capacity, int fused_shared,
+                                         int pad_multiple, int num_permuted_tokens,
+                                         int32_t *map_topk_ids, float *map_topk_probs,
+                                         ep_layout_t *L, void *stream) {
+    cudaStream_t st = as_stream(stream);
+    const int32_t *ids = topk_ids;
+    if (routing_map) {   // the map takes precedence: convert it, then lay out its compact form
+        if (!L || !sizes_ok(T, K, n_experts, fused_shared) ||
+            !padding_ok(T, K, n_experts, fused_shared, pad_multiple, num_permuted_tokens))
+            return EP_ERR_INVALID_ARG;
+        const int rc = launch_map_to_topk(routing_map, dense_probs, T, n_experts, K, map_topk_ids,
+                                          map_topk_probs, st);
+        if (rc != EP_OK) return rc;
+        ids = map_topk_ids;
+    }
+    return launch_layout(ids, T, K, n_experts, n_parts, capacity, fused_shared, pad_multiple,
+                         num_permuted_tokens, L, st, nullptr);
 }
 
 extern "C" int ep_read_status(const ep_layout_t *L, void *stream, int32_t *host_status) {
@@ -892,7 +978,9 @@ extern "C" const char *ep_strerror(int code) {
     switch (code) {
         case EP_OK: return "ok";
         case EP_ERR_INVALID_ARG: return "invalid argument";
-        case EP_ERR_OVERFLOW: return "a logical partition received more tokens than its capacity";
+        case EP_ERR_OVERFLOW:
+            return "a logical partition received more tokens than its capacity, or the rows "
+                   "exceeded the layout's row capacity";
         case EP_ERR_BAD_EXPERT: return "an expert id was outside [-1, n_experts)";
         case EP_ERR_CUDA: return "CUDA error";
         case EP_ERR_TOO_LARGE: return "the sizes need more scratch than the fixed no-allocation array holds";
@@ -973,13 +1061,16 @@ extern "C" int ep_dispatch_layout_noalloc(const int32_t *topk_ids, int T, int K,
     L->P = P;
     L->capacity = capacity;
     L->fused_shared = S;
+    L->pad_multiple = 1;
+    L->row_capacity = 0;
+    const int row_limit = layout_rows(L);
 
     cudaStream_t st = as_stream(stream);
     Workspace ws = carve(scratch, nTiles, E);
     const size_t smem_count = count_smem_bytes(E, P, tt, K);
     ep_layout_count_kernel<<<nTiles, kLayoutThreads, smem_count, st>>>(
-        topk_ids, T, K, E, P, capacity, S, tt, nTiles, magic_of(E / P), ws, L->row_offsets, L->part_tokens,
-        L->status);
+        topk_ids, T, K, E, P, capacity, S, 1, row_limit, tt, nTiles, magic_of(E / P), ws, L->row_offsets,
+        L->part_tokens, L->status);
     rc = launch_result();
     if (rc != EP_OK) return rc;
     size_t smem_rank = sizeof(int) * ((size_t)kLayoutWarps * E + (size_t)tt * K);
@@ -988,7 +1079,7 @@ extern "C" int ep_dispatch_layout_noalloc(const int32_t *topk_ids, int T, int K,
                              (int)smem_rank) != cudaSuccess)
         return EP_ERR_CUDA;
     ep_layout_rank_kernel<<<nTiles, kLayoutThreads, smem_rank, st>>>(
-        topk_ids, T, K, E, S, tt, nTiles, key_bits(E + 1), ws.cnt, L->row_offsets, L->row_of, L->src_info,
-        L->expert_ids);
+        topk_ids, T, K, E, S, 1, row_limit, tt, nTiles, key_bits(E + 1), ws.cnt, L->row_offsets, L->row_of,
+        L->src_info, L->expert_ids);
     return launch_result();
 }

@@ -1,0 +1,135 @@
+// ep_routing.cu -- conversions between the two routing representations: a dense routing map
+// [T, E] (non-zero where token t goes to expert e) with dense probabilities, and compact top-k
+// ids [T, K] (-1 for an unused slot) with per-slot probabilities (fused_a2a page,
+// HybridEPDispatch.forward; token_dispatcher page, _indices_to_multihot).
+//
+// Both kernels give one warp to each token, so a token's row of the map is read or written
+// with consecutive lanes on consecutive experts.
+#include "ep_common.cuh"
+#include "ep_host.h"
+
+namespace ep {
+namespace {
+
+constexpr int kRoutingThreads = 256;
+constexpr int kRoutingWarps = kRoutingThreads / 32;
+
+// Map -> compact.  First pass: count the token's experts (one ballot per 32 experts).  A
+// token with more than K gets the id E in every slot.  Otherwise the second pass writes each
+// set expert at its rank among the set experts (ascending id), and lanes then fill the slots
+// after the last one with -1.
+__global__ void __launch_bounds__(kRoutingThreads)
+ep_map_to_topk_kernel(const uint8_t *__restrict__ map, const float *__restrict__ dense, int T, int E,
+                      int K, int32_t *__restrict__ ids, float *__restrict__ probs) {
+    pdl_begin();
+    const int lane = threadIdx.x & 31;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int t = blockIdx.x * kRoutingWarps + (threadIdx.x >> 5); t < T; t += gridDim.x * kRoutingWarps) {
+        const uint8_t *row = map + (size_t)t * E;
+        int n = 0;
+        for (int e0 = 0; e0 < E; e0 += 32) {
+            const int e = e0 + lane;
+            n += __popc(__ballot_sync(kFullMask, e < E && row[e] != 0));
+        }
+        int32_t *oid = ids + (size_t)t * K;
+        float *op = probs ? probs + (size_t)t * K : nullptr;
+        if (n > K) {
+            if (lane < K) {
+                oid[lane] = E;
+                if (op) op[lane] = 0.0f;
+            }
+            continue;
+        }
+        int before = 0;
+        for (int e0 = 0; e0 < E && before < n; e0 += 32) {
+            const int e = e0 + lane;
+            const bool set = e < E && row[e] != 0;
+            const unsigned b = __ballot_sync(kFullMask, set);
+            if (set) {
+                const int slot = before + __popc(b & lt_mask);
+                oid[slot] = e;
+                if (op) op[slot] = dense ? dense[(size_t)t * E + e] : 0.0f;
+            }
+            before += __popc(b);
+        }
+        if (lane >= n && lane < K) {
+            oid[lane] = -1;
+            if (op) op[lane] = 0.0f;
+        }
+    }
+}
+
+// Compact -> map.  Lane k < K holds the token's slot k; for each expert of its stripe a lane
+// walks the K slots (shuffles, ascending k) and adds the probabilities of the slots naming it.
+__global__ void __launch_bounds__(kRoutingThreads)
+ep_indices_to_multihot_kernel(const int32_t *__restrict__ ids, const float *__restrict__ probs, int T,
+                              int K, int E, uint8_t *__restrict__ map, float *__restrict__ dense) {
+    pdl_begin();
+    const int lane = threadIdx.x & 31;
+    for (int t = blockIdx.x * kRoutingWarps + (threadIdx.x >> 5); t < T; t += gridDim.x * kRoutingWarps) {
+        const int my_id = lane < K ? ids[(size_t)t * K + lane] : -1;
+        const float my_p = (lane < K && probs) ? probs[(size_t)t * K + lane] : 0.0f;
+        for (int e0 = 0; e0 < E; e0 += 32) {
+            const int e = e0 + lane;
+            bool hit = false;
+            float acc = 0.0f;
+            for (int k = 0; k < K; ++k) {
+                const int id = __shfl_sync(kFullMask, my_id, k);
+                const float p = __shfl_sync(kFullMask, my_p, k);
+                if (id == e) {
+                    hit = true;
+                    acc = __fadd_rn(acc, p);
+                }
+            }
+            if (e < E) {
+                map[(size_t)t * E + e] = hit ? 1 : 0;
+                if (dense) dense[(size_t)t * E + e] = acc;
+            }
+        }
+    }
+}
+
+inline int routing_grid(int T) {
+    int grid = (T + kRoutingWarps - 1) / kRoutingWarps;
+    const int cap = 152 * 8;
+    return grid < 1 ? 1 : (grid > cap ? cap : grid);
+}
+
+}  // namespace
+
+int launch_map_to_topk(const uint8_t *routing_map, const float *dense_probs, int T, int E, int K,
+                       int32_t *topk_ids, float *topk_probs, cudaStream_t st) {
+    if (T < 0 || T > kMaxT || E < 1 || E > kMaxE || K < 1 || K > kMaxK) return EP_ERR_INVALID_ARG;
+    if (T > 0 && (!routing_map || !topk_ids)) return EP_ERR_INVALID_ARG;
+    if ((routing_map && !aligned16(routing_map)) || (dense_probs && !aligned16(dense_probs)) ||
+        (topk_ids && !aligned16(topk_ids)) || (topk_probs && !aligned16(topk_probs)))
+        return EP_ERR_INVALID_ARG;
+    if (T == 0) return EP_OK;
+    return launch_pdl(ep_map_to_topk_kernel, dim3(routing_grid(T)), dim3(kRoutingThreads), 0, st,
+                      routing_map, dense_probs, T, E, K, topk_ids, topk_probs);
+}
+
+}  // namespace ep
+
+using namespace ep;
+
+extern "C" int ep_routing_map_to_topk(const uint8_t *routing_map, const float *dense_probs, int T,
+                                      int n_experts, int K, int32_t *topk_ids, float *topk_probs,
+                                      void *stream) {
+    return launch_map_to_topk(routing_map, dense_probs, T, n_experts, K, topk_ids, topk_probs,
+                              as_stream(stream));
+}
+
+extern "C" int ep_indices_to_multihot(const int32_t *topk_ids, const float *topk_probs, int T, int K,
+                                      int n_experts, uint8_t *routing_map, float *dense_probs,
+                                      void *stream) {
+    const int E = n_experts;
+    if (T < 0 || T > kMaxT || E < 1 || E > kMaxE || K < 1 || K > kMaxK) return EP_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_ids || !routing_map)) return EP_ERR_INVALID_ARG;
+    if ((topk_ids && !aligned16(topk_ids)) || (topk_probs && !aligned16(topk_probs)) ||
+        (routing_map && !aligned16(routing_map)) || (dense_probs && !aligned16(dense_probs)))
+        return EP_ERR_INVALID_ARG;
+    if (T == 0) return EP_OK;
+    return launch_pdl(ep_indices_to_multihot_kernel, dim3(routing_grid(T)), dim3(kRoutingThreads), 0,
+                      as_stream(stream), topk_ids, topk_probs, T, K, E, routing_map, dense_probs);
+}

@@ -26,12 +26,13 @@
  *   range) are recorded in the layout's device status word instead, see below.
  * Sizes.  T tokens, K top-k slots, E routed experts, S = 1 when a shared expert is fused
  *   (else 0), G = E + S groups, H hidden size, P logical expert partitions, C their capacity.
- *   R = number of (token, slot) pairs with a valid id + S*T = rows in use, and
- *   R_max = T*K + S*T = rows every dispatched buffer must be sized for, so that no host
- *   synchronisation is ever needed to size an output.  Rows [R, R_max) are never written.
+ *   R = number of (token, slot) pairs with a valid id + S*T = rows in use (plus the padding
+ *   rows when groups are padded, see ep_dispatch_layout_routed), and R_max = rows every
+ *   dispatched buffer must be sized for, so that no host synchronisation is ever needed to
+ *   size an output: T*K + S*T by default, see ep_rows_max.  Rows [R, R_max) are never written.
  * Limits.  0 <= T <= 2^24, 1 <= K <= 32, 1 <= E <= 1024 (K may exceed E: a token may
  *   name an expert in several slots), 1 <= P <= E with E % P == 0,
- *   C >= 0, T*K + S*T < 2^31; H % 16 == 0 and 16 <= H <= 32768.
+ *   C >= 0, R_max < 2^31; H % 16 == 0 and 16 <= H <= 32768.
  */
 #ifndef EP_GB300_H
 #define EP_GB300_H
@@ -47,7 +48,8 @@ extern "C" {
 typedef enum {
     EP_OK = 0,
     EP_ERR_INVALID_ARG = 1,   /* an argument failed a host-side check; nothing was enqueued  */
-    EP_ERR_OVERFLOW = 2,      /* ep_read_status: a partition received more than C tokens     */
+    EP_ERR_OVERFLOW = 2,      /* ep_read_status: a partition received more than C tokens,
+                                 or the rows exceed the layout's row capacity             */
     EP_ERR_BAD_EXPERT = 3,    /* ep_read_status: an expert id was outside [-1, E)            */
     EP_ERR_CUDA = 5,          /* a CUDA call failed (launch error, or the sync in read_status) */
     EP_ERR_TOO_LARGE = 6      /* ep_dispatch_layout_noalloc: the sizes need more scratch than
@@ -82,7 +84,9 @@ typedef enum {
  *                         zero-filled once before its first use; every call leaves it ready
  *                         for the next one.  Calls that share a workspace must not overlap on
  *                         the GPU (use one stream, or one workspace per stream).
- * The remaining fields are recorded by ep_dispatch_layout and checked by the other calls.
+ * The remaining fields are recorded by the layout call and checked by the other calls;
+ * pad_multiple and row_capacity are 1 and 0 (no padding, default R_max) unless the layout was
+ * made by ep_dispatch_layout_routed.
  */
 typedef struct {
     int32_t *row_offsets;
@@ -94,7 +98,17 @@ typedef struct {
     void *workspace;
     size_t workspace_bytes;
     int T, K, E, P, capacity, fused_shared;
+    int pad_multiple, row_capacity;
 } ep_layout_t;
+
+/*
+ * Rows every dispatched buffer (and expert_ids / src_info) must hold for a layout of these
+ * sizes: num_permuted_tokens when it is > 0 (a static row capacity), else
+ * T*K + S*T + (E+S)*(pad_multiple-1), the most rows any routing can need.  pad_multiple <= 1
+ * means no padding.  Returns 0 on invalid sizes.
+ */
+size_t ep_rows_max(int T, int K, int n_experts, int fused_shared, int pad_multiple,
+                   int num_permuted_tokens);
 
 /* Scratch bytes ep_dispatch_layout needs for these sizes (0 on invalid sizes). */
 size_t ep_layout_workspace_bytes(int T, int K, int n_experts, int fused_shared);
@@ -124,6 +138,76 @@ size_t ep_layout_workspace_bytes(int T, int K, int n_experts, int fused_shared);
  */
 int ep_dispatch_layout(const int32_t *topk_ids, int T, int K, int n_experts, int n_parts,
                        int capacity, int fused_shared, ep_layout_t *L, void *stream);
+
+/*
+ * ep_dispatch_layout_routed -- the layout from either routing representation, with optional
+ * per-group padding and a static row capacity.
+ * Defined by: fused_a2a, HybridEPDispatch.forward (a dense Boolean routing map [tokens,
+ * experts] or compact top-k indices, the map taking precedence when both are given;
+ * pad_multiple; num_permuted_tokens, the optional static dispatched-token capacity);
+ * token_dispatcher, TokenDispatcherConfig.moe_router_expert_pad_multiple and _align_up (each
+ * expert's token count rounded up to a multiple), TokenDispatcherConfig.
+ * moe_benchmark_static_routing (a persisted row count keeps the dispatch free of host reads),
+ * and _assert_no_hybridep_overflow (an overflow flag, never a silent truncation).
+ *
+ *   topk_ids       [T*K] int32 device, as for ep_dispatch_layout; read only when routing_map
+ *                  is NULL.
+ *   routing_map    [T*E] uint8 device or NULL: non-zero where token t goes to expert e.  When
+ *                  given it is converted first (exactly as ep_routing_map_to_topk does) into
+ *                  map_topk_ids / map_topk_probs, and the layout is made from map_topk_ids.
+ *   dense_probs    [T*E] fp32 device or NULL: probabilities of the map's entries.
+ *   map_topk_ids   [T*K] int32 device: required when routing_map is given (ignored otherwise).
+ *   map_topk_probs [T*K] fp32 device or NULL: written when routing_map and dense_probs are
+ *                  given; these are the probabilities ep_combine then takes.
+ *   pad_multiple   >= 1 (1: no padding), at most 65536.  Every group's rows (the shared
+ *                  group's too) are followed by padding rows up to a multiple of it:
+ *                  row_offsets[g+1] - row_offsets[g] is a multiple of pad_multiple.  A padding
+ *                  row has expert_ids = its group and src_info = (-1, -1).
+ *   num_permuted_tokens  > 0: the rows the caller's buffers hold (R_max, see ep_rows_max);
+ *                  0: the default R_max.  When the rows needed, row_offsets[G], exceed R_max,
+ *                  EP_STATUS_OVERFLOW is set; rows at or past R_max are not recorded
+ *                  (row_of of their pairs is -1) and no payload is written by later calls.
+ * Everything else (order, partitions, capacity, status) is as for ep_dispatch_layout, which
+ * is this call with routing_map = NULL, pad_multiple = 1, num_permuted_tokens = 0.  Every
+ * dispatch call writes the padding rows of its outputs as the dispatch of an all-zero token,
+ * and ep_combine_bwd writes zero gradients there, so a grouped GEMM over the padded extents
+ * sees zeros; ep_combine and ep_dispatch_bwd never read them.
+ */
+int ep_dispatch_layout_routed(const int32_t *topk_ids, const uint8_t *routing_map,
+                              const float *dense_probs, int T, int K, int n_experts, int n_parts,
+                              int capacity, int fused_shared, int pad_multiple,
+                              int num_permuted_tokens, int32_t *map_topk_ids,
+                              float *map_topk_probs, ep_layout_t *L, void *stream);
+
+/*
+ * ep_routing_map_to_topk -- dense routing map to compact top-k ids.
+ * Defined by: fused_a2a, HybridEPDispatch.forward (routing_map [tokens, experts] Boolean,
+ * probs [tokens, experts] dense; topk_idx [tokens, top_k] with -1 for an unused slot).
+ *   routing_map [T*E] uint8, dense_probs [T*E] fp32 or NULL
+ *   -> topk_ids [T*K] int32: slot j of token t = the j-th expert (ascending id) whose map entry
+ *      is non-zero, -1 after the last one; topk_probs [T*K] fp32 or NULL: the dense
+ *      probability of that entry, 0 for a -1 slot.
+ * A token with more than K experts in the map cannot be written in K slots: every slot of it
+ * gets the id E (and probability 0), which a later layout reports as EP_STATUS_BAD_EXPERT.
+ */
+int ep_routing_map_to_topk(const uint8_t *routing_map, const float *dense_probs, int T,
+                           int n_experts, int K, int32_t *topk_ids, float *topk_probs,
+                           void *stream);
+
+/*
+ * ep_indices_to_multihot -- compact top-k ids to a dense routing map.
+ * Defined by: token_dispatcher, _DeepepManager._indices_to_multihot /
+ * _HybridEPManager._indices_to_multihot ([num_tokens, topk] indices with -1 masked out, and
+ * their probabilities, to a multihot routing map and multihot probabilities).
+ *   topk_ids [T*K] int32, topk_probs [T*K] fp32 or NULL
+ *   -> routing_map [T*E] uint8: 1 where some slot of t names e, else 0;
+ *   -> dense_probs [T*E] fp32 or NULL: the fp32 sum over those slots in ascending k (from +0),
+ *      0 elsewhere (a token naming an expert twice sends it the sum).
+ * Ids outside [0, E) are skipped (the layout is what reports ids outside [-1, E)).  With
+ * topk_probs = grad_probs of ep_combine_bwd this gives the gradient in the dense layout.
+ */
+int ep_indices_to_multihot(const int32_t *topk_ids, const float *topk_probs, int T, int K,
+                           int n_experts, uint8_t *routing_map, float *dense_probs, void *stream);
 
 /*
  * ep_dispatch_nvfp4 -- scatter every token into its rows as NVFP4.
@@ -176,6 +260,21 @@ int ep_dispatch_layout_nvfp4(const int32_t *topk_ids, int T, int K, int n_expert
  */
 int ep_dispatch_bf16(const uint16_t *input_tokens, int hidden_size, const ep_layout_t *L,
                      uint16_t *out, void *stream);
+
+/*
+ * ep_dispatch_fp8 -- scatter every token into its rows as FP8 (E4M3) with one scale per block
+ * of 128 elements.
+ * Defined by: fused_a2a, init_hybrid_ep_buffer, fp8_dispatch (the dispatch may carry FP8
+ * instead of BF16; the pages fix no block size or scale format: this library's reading).
+ *   input_tokens [T*H] bf16, H % 128 == 0
+ *   -> out_fp8    [R_max * H] uint8: E4M3 codes (round to nearest even, saturating to +-448);
+ *   -> out_scales [R_max * H/128] fp32: the factor a consumer multiplies the codes by.
+ * Per block of 128, in fp32 with every operation rounded once: m = max|x|,
+ * s = (m == 0 ? 1 : 448/m, clamped to FLT_MAX), code = E4M3(x * s), scale = 1/s.
+ * All rows of a token receive identical bytes.
+ */
+int ep_dispatch_fp8(const uint16_t *input_tokens, int hidden_size, const ep_layout_t *L,
+                    uint8_t *out_fp8, float *out_scales, void *stream);
 
 /*
  * ep_combine -- probability-weighted gather-reduce of the expert outputs into token order.

@@ -95,3 +95,42 @@ def test_host_validation_without_gpu(libpath):
     assert L.ep_cvt_e2m1(None, None, -1, None) == bad
     assert L.ep_read_status(None, None, None) == bad
     assert ep.strerror(ep.EP_ERR_OVERFLOW).startswith("a logical partition")
+
+
+def test_padding_and_routing_host_validation_without_gpu(libpath):
+    """Host checks of the padded / routed layout, FP8 dispatch and the routing conversions;
+    every call here is rejected before any CUDA call."""
+    import combine_topk_ids_histogram_gb300 as ep
+    L = ep.lib()
+    bad = ep.EP_ERR_INVALID_ARG
+    # rows every buffer holds: T*K + S*T + G*(pad-1), or the static capacity
+    assert L.ep_rows_max(4096, 8, 256, 1, 1, 0) == 4096 * 9
+    assert L.ep_rows_max(4096, 8, 256, 1, 128, 0) == 4096 * 9 + 257 * 127
+    assert L.ep_rows_max(4096, 8, 256, 0, 128, 36864) == 36864
+    assert L.ep_rows_max(4096, 8, 256, 0, 0, 0) == 4096 * 8          # pad <= 1: none
+    assert L.ep_rows_max(4096, 8, 256, 0, 1, -5) == 0
+    assert L.ep_rows_max(4096, 8, 256, 0, 70000, 0) == 0              # pad above 65536
+    assert ep.rows_max(4, 2, 3, True, 4) == 24
+    lay = ep._Layout(row_offsets=256, expert_ids=256, src_info=256, row_of=256, part_tokens=256,
+                     status=256, workspace=256, workspace_bytes=1 << 20)
+    ref = ctypes.byref(lay)
+    args = (4, 2, 8, 1, 4, 0)
+    assert L.ep_dispatch_layout_routed(256, None, None, *args, 0, 0, None, None, ref, None) == bad
+    assert L.ep_dispatch_layout_routed(256, None, None, *args, 1, -1, None, None, ref, None) == bad
+    # a routing map without the buffer for its compact ids
+    assert L.ep_dispatch_layout_routed(None, 256, None, *args, 1, 0, None, None, ref, None) == bad
+    assert L.ep_dispatch_layout_routed(None, 264, None, *args, 1, 0, 256, None, ref, None) == bad
+    assert L.ep_routing_map_to_topk(256, None, 4, 8, 0, 256, None, None) == bad      # K = 0
+    assert L.ep_routing_map_to_topk(256, None, 4, 2000, 2, 256, None, None) == bad   # E too large
+    assert L.ep_routing_map_to_topk(256, None, 4, 8, 2, None, None, None) == bad
+    assert L.ep_indices_to_multihot(256, None, 4, 2, 8, None, None, None) == bad
+    assert L.ep_indices_to_multihot(256, 260, 4, 2, 8, 256, None, None) == bad      # misaligned
+    lay2 = ep._Layout(row_offsets=256, expert_ids=256, src_info=256, row_of=256, part_tokens=256,
+                      status=256, workspace=256, workspace_bytes=1 << 20, T=4, K=2, E=8, P=1,
+                      capacity=4, fused_shared=0, pad_multiple=1, row_capacity=0)
+    r2 = ctypes.byref(lay2)
+    assert L.ep_dispatch_fp8(256, 192, r2, 256, 256, None) == bad     # H % 128 != 0
+    assert L.ep_dispatch_fp8(256, 256, r2, None, 256, None) == bad
+    lay2.pad_multiple = -1
+    assert L.ep_dispatch_fp8(256, 256, r2, 256, 256, None) == bad     # a corrupt layout
+    assert "row capacity" in ep.strerror(ep.EP_ERR_OVERFLOW)
