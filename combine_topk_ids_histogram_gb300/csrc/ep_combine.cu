@@ -17,6 +17,7 @@
 // per token.
 #include "ep_common.cuh"
 #include "ep_host.h"
+#include "ep_padding.cuh"
 
 namespace ep {
 namespace {
@@ -107,7 +108,8 @@ template <int KMAX>
 __global__ void __launch_bounds__(kCombineThreads)
 ep_combine_bwd_kernel(const uint16_t *__restrict__ g, const uint16_t *__restrict__ y,
                       const float *__restrict__ probs, int T, int H, int K, int E, int S, int R_max,
-                      const int32_t *__restrict__ row_of, const int32_t *__restrict__ row_offsets,
+                      int nfill, int pad, const int32_t *__restrict__ row_of,
+                      const int32_t *__restrict__ row_offsets, const int32_t *__restrict__ src_info,
                       const int32_t *__restrict__ status, uint16_t *__restrict__ grad_y,
                       float *__restrict__ grad_p) {
     __shared__ int s_rows[KMAX];
@@ -115,8 +117,13 @@ ep_combine_bwd_kernel(const uint16_t *__restrict__ g, const uint16_t *__restrict
     __shared__ float s_red[kCombineThreads / 32][KMAX];
     pdl_begin();
     if (load_status(status)) return;
+    if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: zero gradient rows
+        fill_group_padding(blockIdx.x, pad, row_offsets, src_info, PadFill{grad_y, 2 * H, 0u},
+                           PadFill{nullptr, 0, 0u}, PadFill{nullptr, 0, 0u});
+        return;
+    }
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int t = blockIdx.x;
+    const int t = blockIdx.x - nfill;
     if (tid < KMAX) {
         int r = -1;
         float p = 0.0f;
@@ -239,25 +246,21 @@ extern "C" int ep_combine_bwd(const uint16_t *grad_out, const uint16_t *expert_o
     const void *ptrs[] = {grad_out, expert_out, probs, grad_expert_out, grad_probs};
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return EP_ERR_INVALID_ARG;
+    if (L->T == 0) return EP_OK;
     cudaStream_t st = as_stream(stream);
-    if (L->T > 0) {
-        const int K = L->K;
-        const int R_max = layout_rows(L);
-        int rc;
+    const int K = L->K;
+    const int R_max = layout_rows(L);
+    const int nfill = fill_ctas(L);   // padding rows of a padded layout get a zero gradient
 #define EP_BWD_CASE(KM)                                                                        \
-    rc = launch_pdl(ep_combine_bwd_kernel<KM>, dim3(L->T), dim3(kCombineThreads), 0, st,       \
-                    grad_out, expert_out, probs, L->T, H, K, L->E, L->fused_shared, R_max,     \
-                    (const int32_t *)L->row_of, (const int32_t *)L->row_offsets,               \
-                    (const int32_t *)L->status, grad_expert_out, grad_probs)
-        if (K <= 2) EP_BWD_CASE(2);
-        else if (K <= 4) EP_BWD_CASE(4);
-        else if (K <= 8) EP_BWD_CASE(8);
-        else if (K <= 16) EP_BWD_CASE(16);
-        else EP_BWD_CASE(32);
+    return launch_pdl(ep_combine_bwd_kernel<KM>, dim3(L->T + nfill), dim3(kCombineThreads), 0, st, \
+                      grad_out, expert_out, probs, L->T, H, K, L->E, L->fused_shared, R_max,   \
+                      nfill, L->pad_multiple, (const int32_t *)L->row_of,                      \
+                      (const int32_t *)L->row_offsets, (const int32_t *)L->src_info,           \
+                      (const int32_t *)L->status, grad_expert_out, grad_probs)
+    if (K <= 2) EP_BWD_CASE(2);
+    if (K <= 4) EP_BWD_CASE(4);
+    if (K <= 8) EP_BWD_CASE(8);
+    if (K <= 16) EP_BWD_CASE(16);
+    EP_BWD_CASE(32);
 #undef EP_BWD_CASE
-        if (rc != EP_OK) return rc;
-    }
-    // a padding row's gradient is zero
-    return launch_fill_padding(L, PadFill{grad_expert_out, 2 * H, 0u}, PadFill{nullptr, 0, 0u},
-                               PadFill{nullptr, 0, 0u}, st);
 }

@@ -13,6 +13,7 @@
 #include "ep_common.cuh"
 #include "ep_async.cuh"
 #include "ep_host.h"
+#include "ep_padding.cuh"
 
 namespace ep {
 namespace {
@@ -53,11 +54,12 @@ __device__ __forceinline__ float absmax8(uint4 v) {
 template <int BPT, int MAXT, int MINB>
 __global__ void __launch_bounds__(MAXT, MINB)
 ep_dispatch_nvfp4_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int E, int S, int G, int R_max,
-                         int early,
+                         int early, int nfill, int pad,
                          const int32_t *__restrict__ row_of, const int32_t *__restrict__ row_offsets,
+                         const int32_t *__restrict__ src_info,
                          const int32_t *__restrict__ status, uint8_t *__restrict__ out_fp4,
                          uint8_t *__restrict__ out_scales, uint16_t *__restrict__ out_inv,
-                         int32_t *__restrict__ scales_offsets) {
+                         int32_t *__restrict__ scales_offsets, PadFill f0, PadFill f1, PadFill f2) {
     __shared__ int s_rows[kMaxRowsPerToken];
     __shared__ float s_red[32];
     // early == 0: wait for the previous kernel first; the token row, the row indices and the
@@ -66,8 +68,12 @@ ep_dispatch_nvfp4_kernel(const uint16_t *__restrict__ x, int T, int H, int K, in
     //             only once every earlier kernel had completed), so x is read and quantised
     //             while the layout still runs, and the layout's outputs are read after the wait.
     if (!early) pdl_begin();
+    if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: one group's padding rows
+        if (!load_status(status)) fill_group_padding_call(blockIdx.x, pad, row_offsets, src_info, f0, f1, f2);
+        return;
+    }
     const int tid = threadIdx.x;
-    const int t = blockIdx.x;
+    const int t = blockIdx.x - nfill;
     const int nth = H / (16 * BPT);
     const bool active = tid < nth && t < T;
     uint4 v[2 * BPT];
@@ -148,13 +154,19 @@ ep_dispatch_nvfp4_kernel(const uint16_t *__restrict__ x, int T, int H, int K, in
 
 __global__ void __launch_bounds__(256)
 ep_dispatch_bf16_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int E, int S, int R_max,
-                        const int32_t *__restrict__ row_of, const int32_t *__restrict__ row_offsets,
-                        const int32_t *__restrict__ status, uint16_t *__restrict__ out) {
+                        int nfill, int pad, const int32_t *__restrict__ row_of,
+                        const int32_t *__restrict__ row_offsets, const int32_t *__restrict__ src_info,
+                        const int32_t *__restrict__ status, uint16_t *__restrict__ out, PadFill f0) {
     __shared__ int s_rows[kMaxRowsPerToken];
     pdl_begin();
     if (load_status(status)) return;
+    if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: one group's padding rows
+        fill_group_padding_call(blockIdx.x, pad, row_offsets, src_info, f0, PadFill{nullptr, 0, 0u},
+                           PadFill{nullptr, 0, 0u});
+        return;
+    }
     const int tid = threadIdx.x;
-    const int t = blockIdx.x;
+    const int t = blockIdx.x - nfill;
     const int nrows = K + S;
     if (tid < K) s_rows[tid] = row_of[(size_t)t * K + tid];
     else if (tid == K && S) s_rows[K] = row_offsets[E] + t;
@@ -174,21 +186,29 @@ ep_dispatch_bf16_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int
 // FP8 dispatch: one CTA per token, one thread per 32 elements, so the four threads of a
 // 128-element block share its maximum through two shuffles.  Per block, in fp32 with every
 // operation rounded once: s = 448 / max|x| (1 for an all-zero block, FLT_MAX if it overflows),
-// code = E4M3(x * s) by the hardware conversion, scale = 1 / s.  The row is read once and its
-// 32 code bytes per thread are stored to each of the token's K (+1 shared) rows.
+// code = E4M3(x * s) by the hardware conversion, scale = 1 / s.  The row is read once.  Each
+// lane's 32 code bytes are then exchanged within the warp (once per token) so that each of the
+// warp's two 16-byte stores per destination row covers 512 contiguous bytes, and the same
+// words are stored to each of the token's K (+1 shared) rows.
 // ---------------------------------------------------------------------------------------
 constexpr int kFp8Block = 128;
 
 template <int MAXT, int MINB>
 __global__ void __launch_bounds__(MAXT, MINB)
 ep_dispatch_fp8_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int E, int S, int R_max,
-                       const int32_t *__restrict__ row_of, const int32_t *__restrict__ row_offsets,
+                       int nfill, int pad, const int32_t *__restrict__ row_of,
+                       const int32_t *__restrict__ row_offsets, const int32_t *__restrict__ src_info,
                        const int32_t *__restrict__ status, uint8_t *__restrict__ out_fp8,
-                       float *__restrict__ out_scales) {
+                       float *__restrict__ out_scales, PadFill f0, PadFill f1) {
     __shared__ int s_rows[kMaxRowsPerToken];
     pdl_begin();
+    if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: one group's padding rows
+        if (!load_status(status))
+            fill_group_padding_call(blockIdx.x, pad, row_offsets, src_info, f0, f1, PadFill{nullptr, 0, 0u});
+        return;
+    }
     const int tid = threadIdx.x;
-    const int t = blockIdx.x;
+    const int t = blockIdx.x - nfill;
     const bool active = tid < H / 32;
     uint4 v[4];
     if (active) {
@@ -208,7 +228,6 @@ ep_dispatch_fp8_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int 
     m = fmaxf(m, __shfl_xor_sync(kFullMask, m, 1));   // the four threads of the block
     m = fmaxf(m, __shfl_xor_sync(kFullMask, m, 2));
     __syncthreads();
-    if (!active) return;
     float sc = 1.0f;
     if (m != 0.0f) {
         sc = __fdiv_rn(448.0f, m);
@@ -225,64 +244,32 @@ ep_dispatch_fp8_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int 
             cvt_e4m3x2(__fmul_rn(bf16_lo(w[2 * q + 1]), sc), __fmul_rn(bf16_hi(w[2 * q + 1]), sc));
         c[q] = lo | (hi << 16);
     }
+    // Lane l holds bytes [32l, 32l + 32) of its warp's 1 KiB of codes.  After the exchange, lane l
+    // holds bytes [16l, 16l + 16) (w1) and [512 + 16l, 512 + 16l + 16) (w2): the 16-byte half
+    // (l & 1) of lanes l/2 and 16 + l/2.
+    const int lane = tid & 31;
+    const bool odd = lane & 1;
+    uint32_t w1[4], w2[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t a1 = __shfl_sync(kFullMask, c[i], lane >> 1);
+        const uint32_t b1 = __shfl_sync(kFullMask, c[4 + i], lane >> 1);
+        const uint32_t a2 = __shfl_sync(kFullMask, c[i], 16 + (lane >> 1));
+        const uint32_t b2 = __shfl_sync(kFullMask, c[4 + i], 16 + (lane >> 1));
+        w1[i] = odd ? b1 : a1;
+        w2[i] = odd ? b2 : a2;
+    }
+    const int off1 = (tid - lane) * 32 + lane * 16;   // byte offsets in the row
+    const int off2 = off1 + 512;
     const int nrows = K + S;
     const int nblk = H / kFp8Block;
     for (int k = 0; k < nrows; ++k) {
         const int r = s_rows[k];
         if (r < 0 || r >= R_max) continue;
-        uint8_t *dst = out_fp8 + (size_t)r * H + (size_t)tid * 32;
-        st_stream(dst, make_uint4(c[0], c[1], c[2], c[3]));
-        st_stream(dst + 16, make_uint4(c[4], c[5], c[6], c[7]));
-        if ((tid & 3) == 0) __stcs(out_scales + (size_t)r * nblk + (tid >> 2), scale);
-    }
-}
-
-// ---------------------------------------------------------------------------------------
-// Padding rows of a padded layout: every row below min(row_offsets[G], R_max) whose source
-// token is -1 receives the bytes an all-zero token dispatches to (up to three buffers).  Each
-// CTA takes kFillRows rows at a time: one thread per row tests it, the padding rows are listed
-// in shared memory, and one warp writes each listed row.
-// ---------------------------------------------------------------------------------------
-constexpr int kFillRows = 256;
-
-__device__ __forceinline__ void fill_row(const PadFill &f, int row, int lane) {
-    if (!f.ptr) return;
-    unsigned char *p = static_cast<unsigned char *>(f.ptr) + (size_t)row * f.row_bytes;
-    if (f.row_bytes % 16 == 0) {
-        const uint4 v = make_uint4(f.pattern, f.pattern, f.pattern, f.pattern);
-        for (int i = lane; i < f.row_bytes / 16; i += 32) reinterpret_cast<uint4 *>(p)[i] = v;
-    } else if (f.row_bytes % 4 == 0) {
-        for (int i = lane; i < f.row_bytes / 4; i += 32) reinterpret_cast<uint32_t *>(p)[i] = f.pattern;
-    } else {
-        for (int i = lane; i < f.row_bytes / 2; i += 32)
-            reinterpret_cast<uint16_t *>(p)[i] = (uint16_t)f.pattern;
-    }
-}
-
-__global__ void __launch_bounds__(kFillRows)
-ep_fill_padding_kernel(const int32_t *__restrict__ src_info, const int32_t *__restrict__ row_offsets,
-                       int G, int R_max, const int32_t *__restrict__ status, PadFill f0, PadFill f1,
-                       PadFill f2) {
-    __shared__ int s_list[kFillRows];
-    __shared__ int s_n;
-    pdl_begin();
-    if (load_status(status)) return;
-    const int end = min(row_offsets[G], R_max);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int base = blockIdx.x * kFillRows; base < end; base += gridDim.x * kFillRows) {
-        if (tid == 0) s_n = 0;
-        __syncthreads();
-        const int r = base + tid;
-        if (r < end && src_info[2 * (size_t)r] < 0) s_list[atomicAdd(&s_n, 1)] = r;
-        __syncthreads();
-        const int n = s_n;
-        for (int i = warp; i < n; i += kFillRows / 32) {
-            const int row = s_list[i];
-            fill_row(f0, row, lane);
-            fill_row(f1, row, lane);
-            fill_row(f2, row, lane);
-        }
-        __syncthreads();
+        uint8_t *dst = out_fp8 + (size_t)r * H;
+        if (off1 < H) st_stream(dst + off1, make_uint4(w1[0], w1[1], w1[2], w1[3]));
+        if (off2 < H) st_stream(dst + off2, make_uint4(w2[0], w2[1], w2[2], w2[3]));
+        if (active && (tid & 3) == 0) __stcs(out_scales + (size_t)r * nblk + (tid >> 2), scale);
     }
 }
 
@@ -463,6 +450,11 @@ namespace {
 int launch_nvfp4(const uint16_t *input_tokens, int H, const ep_layout_t *L, uint8_t *out_fp4,
                  uint8_t *out_scales, uint16_t *out_rowwise_inv_scale, int32_t *scales_offsets,
                  int early, cudaStream_t st) {
+    // padding rows (padded layouts; the fused call's layout is never padded): codes 0, block
+    // scales 0, inverse global scale bf16(1/1) = 0x3F80 -- the dispatch of an all-zero token
+    const int nfill = early ? 0 : fill_ctas(L);
+    const PadFill f0{out_fp4, H / 2, 0u}, f1{out_scales, H / 16, 0u},
+        f2{out_rowwise_inv_scale, 2, 0x3F803F80u};
     if (!layout_ok(L) || !hidden_ok(H)) return EP_ERR_INVALID_ARG;
     const int bpt = (H % 32 == 0) ? 2 : 1;
     const int nth = H / (16 * bpt);
@@ -475,15 +467,16 @@ int launch_nvfp4(const uint16_t *input_tokens, int H, const ep_layout_t *L, uint
         if (p && !aligned16(p)) return EP_ERR_INVALID_ARG;
     // enough threads to load the K (+1 shared) row indices of the token
     const int threads = max((nth + 31) / 32 * 32, (L->K + 1 + 31) / 32 * 32);
-    const int grid = L->T > 0 ? L->T : 1;
+    const int grid = (L->T > 0 ? L->T : 1) + nfill;
     const int G = L->E + L->fused_shared;
     const int R_max = layout_rows(L);
     const int32_t *row_of = L->row_of, *row_offsets = L->row_offsets, *status = L->status;
+    const int32_t *src_info = L->src_info;
 #define EP_NVFP4_LAUNCH(BPT, MAXT, MINB)                                                        \
     return launch_pdl(ep_dispatch_nvfp4_kernel<BPT, MAXT, MINB>, dim3(grid), dim3(threads), 0, st, \
-                      input_tokens, L->T, H, L->K, L->E, L->fused_shared, G, R_max, early, row_of, \
-                      row_offsets, status, out_fp4, out_scales, out_rowwise_inv_scale,          \
-                      scales_offsets)
+                      input_tokens, L->T, H, L->K, L->E, L->fused_shared, G, R_max, early, nfill, \
+                      L->pad_multiple, row_of, row_offsets, src_info, status, out_fp4, out_scales, \
+                      out_rowwise_inv_scale, scales_offsets, f0, f1, f2)
     // Up to 256 threads (H <= 8192): 5 such CTAs per SM without spilling.
     if (bpt == 2 && threads <= 256) EP_NVFP4_LAUNCH(2, 256, 5);
     if (bpt == 2) EP_NVFP4_LAUNCH(2, 1024, 1);
@@ -494,31 +487,13 @@ int launch_nvfp4(const uint16_t *input_tokens, int H, const ep_layout_t *L, uint
 
 }  // namespace
 
-int launch_fill_padding(const ep_layout_t *L, PadFill a, PadFill b, PadFill c, cudaStream_t st) {
-    if (!layout_padded(L)) return EP_OK;
-    const int R_max = layout_rows(L);
-    if (R_max == 0) return EP_OK;
-    int grid = (R_max + kFillRows - 1) / kFillRows;
-    const int cap = resident_blocks(ep_fill_padding_kernel, kFillRows, 0);
-    if (cap > 0 && grid > cap) grid = cap;
-    return launch_pdl(ep_fill_padding_kernel, dim3(grid), dim3(kFillRows), 0, st,
-                      (const int32_t *)L->src_info, (const int32_t *)L->row_offsets,
-                      L->E + L->fused_shared, R_max, (const int32_t *)L->status, a, b, c);
-}
-
 }  // namespace ep
 
 extern "C" int ep_dispatch_nvfp4(const uint16_t *input_tokens, int hidden_size, const ep_layout_t *L,
                                  uint8_t *out_fp4, uint8_t *out_scales, uint16_t *out_rowwise_inv_scale,
                                  int32_t *scales_offsets, void *stream) {
-    cudaStream_t st = as_stream(stream);
-    const int rc = launch_nvfp4(input_tokens, hidden_size, L, out_fp4, out_scales,
-                                out_rowwise_inv_scale, scales_offsets, 0, st);
-    if (rc != EP_OK) return rc;
-    // padding rows: codes 0, block scales 0, inverse global scale bf16(1/1) = 0x3F80
-    const int H = hidden_size;
-    return launch_fill_padding(L, PadFill{out_fp4, H / 2, 0u}, PadFill{out_scales, H / 16, 0u},
-                               PadFill{out_rowwise_inv_scale, 2, 0x3F803F80u}, st);
+    return launch_nvfp4(input_tokens, hidden_size, L, out_fp4, out_scales, out_rowwise_inv_scale,
+                        scales_offsets, 0, as_stream(stream));
 }
 
 extern "C" int ep_dispatch_layout_nvfp4(const int32_t *topk_ids, int T, int K, int n_experts,
@@ -556,16 +531,13 @@ extern "C" int ep_dispatch_bf16(const uint16_t *input_tokens, int hidden_size, c
     if (!layout_ok(L) || !hidden_ok(H)) return EP_ERR_INVALID_ARG;
     if (L->T > 0 && (!input_tokens || !out)) return EP_ERR_INVALID_ARG;
     if ((input_tokens && !aligned16(input_tokens)) || (out && !aligned16(out))) return EP_ERR_INVALID_ARG;
-    cudaStream_t st = as_stream(stream);
-    if (L->T > 0) {
-        const int rc = launch_pdl(ep_dispatch_bf16_kernel, dim3(L->T), dim3(256), 0, st, input_tokens,
-                                  L->T, H, L->K, L->E, L->fused_shared, layout_rows(L),
-                                  (const int32_t *)L->row_of, (const int32_t *)L->row_offsets,
-                                  (const int32_t *)L->status, out);
-        if (rc != EP_OK) return rc;
-    }
-    return launch_fill_padding(L, PadFill{out, 2 * H, 0u}, PadFill{nullptr, 0, 0u},
-                               PadFill{nullptr, 0, 0u}, st);
+    if (L->T == 0) return EP_OK;
+    const int nfill = fill_ctas(L);   // padding rows: zeros
+    return launch_pdl(ep_dispatch_bf16_kernel, dim3(L->T + nfill), dim3(256), 0, as_stream(stream),
+                      input_tokens, L->T, H, L->K, L->E, L->fused_shared, layout_rows(L), nfill,
+                      L->pad_multiple, (const int32_t *)L->row_of, (const int32_t *)L->row_offsets,
+                      (const int32_t *)L->src_info, (const int32_t *)L->status, out,
+                      PadFill{out, 2 * H, 0u});
 }
 
 extern "C" int ep_dispatch_fp8(const uint16_t *input_tokens, int hidden_size, const ep_layout_t *L,
@@ -576,27 +548,24 @@ extern "C" int ep_dispatch_fp8(const uint16_t *input_tokens, int hidden_size, co
     const void *ptrs[] = {input_tokens, out_fp8, out_scales};
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return EP_ERR_INVALID_ARG;
+    if (L->T == 0) return EP_OK;
     cudaStream_t st = as_stream(stream);
-    if (L->T > 0) {
-        const int threads = max(H / 32, 32 * ((L->K + 1 + 31) / 32));   // H % 128 == 0: whole warps
-        const int R_max = layout_rows(L);
-        int rc;
-        if (threads <= 256)
-            rc = launch_pdl(ep_dispatch_fp8_kernel<256, 5>, dim3(L->T), dim3(threads), 0, st,
-                            input_tokens, L->T, H, L->K, L->E, L->fused_shared, R_max,
-                            (const int32_t *)L->row_of, (const int32_t *)L->row_offsets,
-                            (const int32_t *)L->status, out_fp8, out_scales);
-        else
-            rc = launch_pdl(ep_dispatch_fp8_kernel<1024, 1>, dim3(L->T), dim3(threads), 0, st,
-                            input_tokens, L->T, H, L->K, L->E, L->fused_shared, R_max,
-                            (const int32_t *)L->row_of, (const int32_t *)L->row_offsets,
-                            (const int32_t *)L->status, out_fp8, out_scales);
-        if (rc != EP_OK) return rc;
-    }
+    const int threads = max(H / 32, 32 * ((L->K + 1 + 31) / 32));   // H % 128 == 0: whole warps
+    const int R_max = layout_rows(L);
+    const int nfill = fill_ctas(L);
     // padding rows: codes 0 and the scale of an all-zero block, 1.0f
-    return launch_fill_padding(L, PadFill{out_fp8, H, 0u},
-                               PadFill{out_scales, 4 * (H / kFp8Block), 0x3F800000u},
-                               PadFill{nullptr, 0, 0u}, st);
+    const PadFill f0{out_fp8, H, 0u}, f1{out_scales, 4 * (H / kFp8Block), 0x3F800000u};
+    if (threads <= 256)
+        return launch_pdl(ep_dispatch_fp8_kernel<256, 5>, dim3(L->T + nfill), dim3(threads), 0, st,
+                          input_tokens, L->T, H, L->K, L->E, L->fused_shared, R_max, nfill,
+                          L->pad_multiple, (const int32_t *)L->row_of, (const int32_t *)L->row_offsets,
+                          (const int32_t *)L->src_info, (const int32_t *)L->status, out_fp8,
+                          out_scales, f0, f1);
+    return launch_pdl(ep_dispatch_fp8_kernel<1024, 1>, dim3(L->T + nfill), dim3(threads), 0, st,
+                      input_tokens, L->T, H, L->K, L->E, L->fused_shared, R_max, nfill,
+                      L->pad_multiple, (const int32_t *)L->row_of, (const int32_t *)L->row_offsets,
+                      (const int32_t *)L->src_info, (const int32_t *)L->status, out_fp8, out_scales,
+                      f0, f1);
 }
 
 extern "C" int ep_cvt_e2m1(const float *in, uint8_t *codes, long n, void *stream) {

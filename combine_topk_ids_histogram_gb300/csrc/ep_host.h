@@ -135,16 +135,4 @@ int launch_layout(const int32_t *topk_ids, int T, int K, int E, int P, int capac
 int launch_map_to_topk(const uint8_t *routing_map, const float *dense_probs, int T, int E, int K,
                        int32_t *topk_ids, float *topk_probs, cudaStream_t st);
 
-// One buffer whose padding rows a dispatch fills: `row_bytes` per row (even), every 32-bit
-// word of a padding row set to `pattern` (16-bit periodic when row_bytes % 4 != 0).
-struct PadFill {
-    void *ptr;
-    int row_bytes;
-    uint32_t pattern;
-};
-
-// Enqueues the fill of the padding rows of up to three buffers of a padded layout
-// (ep_dispatch.cu); EP_OK without a launch when the layout has no padding.
-int launch_fill_padding(const ep_layout_t *L, PadFill a, PadFill b, PadFill c, cudaStream_t st);
-
 }  // namespace ep

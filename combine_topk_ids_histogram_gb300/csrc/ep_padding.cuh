@@ -1,0 +1,69 @@
+// ep_padding.cuh -- the padding rows of a padded layout (token_dispatcher page,
+// TokenDispatcherConfig.moe_router_expert_pad_multiple), written by extra CTAs that lead the
+// grids of the dispatch kernels and of the combine backward kernel, so the fill runs
+// alongside the per-token work instead of after it.
+#pragma once
+
+#include "ep_common.cuh"
+
+namespace ep {
+
+// One buffer whose padding rows a kernel fills: `row_bytes` per row (even), every 32-bit word
+// of a padding row set to `pattern` (16-bit periodic when row_bytes % 4 != 0).  A null ptr
+// means no buffer.
+struct PadFill {
+    void *ptr;
+    int row_bytes;
+    uint32_t pattern;
+};
+
+__device__ __forceinline__ void fill_row(const PadFill &f, int row, int lane) {
+    if (!f.ptr) return;
+    unsigned char *p = static_cast<unsigned char *>(f.ptr) + (size_t)row * f.row_bytes;
+    if (f.row_bytes % 16 == 0) {
+        const uint4 v = make_uint4(f.pattern, f.pattern, f.pattern, f.pattern);
+        for (int i = lane; i < f.row_bytes / 16; i += 32) st_stream(reinterpret_cast<uint4 *>(p) + i, v);
+    } else if (f.row_bytes % 4 == 0) {
+        for (int i = lane; i < f.row_bytes / 4; i += 32) reinterpret_cast<uint32_t *>(p)[i] = f.pattern;
+    } else {
+        for (int i = lane; i < f.row_bytes / 2; i += 32)
+            reinterpret_cast<uint16_t *>(p)[i] = (uint16_t)f.pattern;
+    }
+}
+
+// Group g's padding rows close the group: [first, row_offsets[g+1]), at most pad - 1 of them,
+// where `first` is the lowest row among the group's last pad - 1 rows whose source token is -1
+// (every row before it is one of the group's routed rows).  The whole CTA finds `first`, then
+// its warps write the rows.  Call only while the layout's status word is 0 (then every row is
+// below R_max).
+__device__ __forceinline__ void fill_group_padding(int g, int pad, const int32_t *__restrict__ row_offsets,
+                                                   const int32_t *__restrict__ src_info, const PadFill &f0,
+                                                   const PadFill &f1, const PadFill &f2) {
+    __shared__ int s_first;
+    const int hi = row_offsets[g + 1];
+    const int lo = max(row_offsets[g], hi - (pad - 1));
+    if (threadIdx.x == 0) s_first = hi;
+    __syncthreads();
+    for (int r = lo + threadIdx.x; r < hi; r += blockDim.x)
+        if (src_info[2 * (size_t)r] < 0) atomicMin(&s_first, r);
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int r = s_first + warp; r < hi; r += nw) {
+        fill_row(f0, r, lane);
+        fill_row(f1, r, lane);
+        fill_row(f2, r, lane);
+    }
+}
+
+// The same as a separate function, for kernels whose own register allocation should not
+// carry the fill's.
+static __device__ __noinline__ void fill_group_padding_call(int g, int pad, const int32_t *__restrict__ row_offsets,
+                                                     const int32_t *__restrict__ src_info, PadFill f0,
+                                                     PadFill f1, PadFill f2) {
+    fill_group_padding(g, pad, row_offsets, src_info, f0, f1, f2);
+}
+
+// Extra leading CTAs of a grid for a layout's padding rows: one per group when padded.
+inline int fill_ctas(const ep_layout_t *L) { return L->pad_multiple > 1 ? L->E + L->fused_shared : 0; }
+
+}  // namespace ep

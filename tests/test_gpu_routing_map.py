@@ -78,7 +78,10 @@ def test_too_dense_map_is_reported_by_the_layout(ep):
     m = np.zeros((50, 16), np.uint8)
     m[:, 3] = 1
     m[7, :6] = 1                          # 6 experts with K = 4
-    L, ids, _ = ep.dispatch_layout_routed(16, routing_map=dev(m), K=4)
+    L = ep.Layout(50, 4, 16)
+    L.expert_ids.fill_(CANARY32)
+    L.src_info.fill_(CANARY32)
+    _, ids, _ = ep.dispatch_layout_routed(16, routing_map=dev(m), K=4, out=L)
     assert ep.read_status(L) == ep.STATUS_BAD_EXPERT
     assert ids.cpu().numpy()[7].tolist() == [16] * 4
     ref = oracle.layout(oracle.routing_map_to_topk(m, None, 4)[0], 16)
