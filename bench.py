@@ -91,7 +91,7 @@ def load_peaks() -> tuple[float, str]:
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("ep_common.cuh", "ep_combine.cu"):
+    for f in ("ep_common.cuh", "ep_padding.cuh", "ep_combine.cu"):   # device code of combine's unit
         with open(os.path.join(ROOT, "combine_topk_ids_histogram_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -636,7 +636,7 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
     cluster_sync_all();
 
     //    cluster totals per expert (thread tid owns experts kClExpertsPerThread*tid + q), and
-    //    their extents: the totals rounded up to a multiple of pad
+    //    their extents: each total padded to the next multiple of pad
     int mine = 0, mine_local = 0;
     int before[kClExpertsPerThread], total[kClExpertsPerThread];
 #pragma unroll

@@ -134,7 +134,7 @@ float oracle_e4m3_decode(uint8_t code)
  *
  * 1. An id outside [-1, E) sets BAD_EXPERT and is then treated as an unused slot.
  * 2. counts[e] = #{(t,k): id = e}; with a fused shared expert, group E holds one row per token.
- * 3. extent[g] = counts[g] rounded up to a multiple of pad (pad = 1: no padding);
+ * 3. extent[g] = the smallest multiple of pad that is >= counts[g] (pad = 1: no padding);
  *    row_offsets = exclusive scan of the extents over the G = E + S groups.
  * 4. Rows of group e are its (t,k) pairs in ascending flat index t*K+k: a stable sort of the
  *    flat indices keyed by expert id; the i-th pair of group e is row row_offsets[e] + i.

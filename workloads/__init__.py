@@ -17,7 +17,7 @@ Recipe (all draws from ``numpy.random.Generator(PCG64(seed))``):
 * expert outputs ``y`` and gradients: standard normal in float32 rounded to bf16.
 
 The "balanced" router draws nothing: slot k of token t names expert (t*K + k) mod E with
-probability 1/K (static routing for benchmarks, so every dispatch permutes the same row count).
+probability 1/K (static benchmark routing: the row count is identical on every dispatch).
 
 Seeds per config index c: x 1000+c, logits 2000+c, expert bias 3000+c, Zipf draws 4000+c,
 outlier / zero-row choice 5000+c, grad_out 6000+c, expert outputs 7000+c, grad rows 8000+c.
@@ -68,8 +68,9 @@ CONFIGS: dict[str, Config] = {
     "mixtral": Config(4, "mixtral", T=16384, H=4096, E=8, K=2, router="zipf"),
     "dsv3_large": Config(5, "dsv3_large", T=32768, H=7168, E=256, K=8, P=8, C=20000,
                          router="hot", zero_frac=0.001, rerun_C=40000),
-    # benchmark static routing: forced-balanced, no noise, so every dispatch has the same row
-    # count (T*K/E = 128 rows per expert), passed as a static row capacity; groups padded to 128
+    # benchmark static routing: balanced and noise-free, so the row count (T*K/E = 128 rows per
+    # expert, plus the shared rows) is the same on every dispatch and is passed as a static row
+    # capacity; groups padded to 128
     "dsv3_static": Config(6, "dsv3_static", T=4096, H=7168, E=256, K=8, S=1, P=8, C=4096,
                           router="balanced", pad_multiple=128, num_permuted_tokens=4096 * 8 + 4096),
 }
