@@ -3,7 +3,7 @@
 // ids [T, K] (-1 for an unused slot) with per-slot probabilities (fused_a2a page,
 // HybridEPDispatch.forward; token_dispatcher page, _indices_to_multihot).
 //
-// Both kernels give one warp to each token, so a token's row of the map is read or written
+// Both directions give one warp to each token, so a token's row of the map is read or written
 // with consecutive lanes on consecutive experts.
 #include "ep_common.cuh"
 #include "ep_host.h"
@@ -59,6 +59,73 @@ ep_map_to_topk_kernel(const uint8_t *__restrict__ map, const float *__restrict__
     }
 }
 
+// Map -> compact when E % 16 == 0: each lane reads 16 map bytes per 16-byte load (a 16-bit
+// mask of set experts), a warp scan of the masks' counts gives each lane's first slot, and
+// each lane writes its set experts in ascending order.  One pass of at most E/512 loads per
+// lane; the ids past the token's last expert are written -1 after the total is known.
+__device__ __forceinline__ unsigned byte_mask16(uint4 v) {
+    unsigned m = 0;
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        if ((w[i >> 2] >> (8 * (i & 3))) & 0xffu) m |= 1u << i;
+    return m;
+}
+
+__global__ void __launch_bounds__(kRoutingThreads)
+ep_map_to_topk_wide_kernel(const uint8_t *__restrict__ map, const float *__restrict__ dense, int T,
+                           int E, int K, int32_t *__restrict__ ids, float *__restrict__ probs) {
+    pdl_begin();
+    const int lane = threadIdx.x & 31;
+    const int nchunk = E / 16;                    // 16-byte chunks per map row
+    for (int t = blockIdx.x * kRoutingWarps + (threadIdx.x >> 5); t < T; t += gridDim.x * kRoutingWarps) {
+        const uint4 *row = reinterpret_cast<const uint4 *>(map + (size_t)t * E);
+        unsigned m0 = 0, m1 = 0;                  // chunks lane and lane + 32 (E <= 1024)
+        if (lane < nchunk) m0 = byte_mask16(__ldg(row + lane));
+        if (lane + 32 < nchunk) m1 = byte_mask16(__ldg(row + lane + 32));
+        const int c0 = __popc(m0), c1 = __popc(m1);
+        int incl0 = c0, incl1 = c1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int a = __shfl_up_sync(kFullMask, incl0, o);
+            const int b = __shfl_up_sync(kFullMask, incl1, o);
+            if (lane >= o) {
+                incl0 += a;
+                incl1 += b;
+            }
+        }
+        const int tot0 = __shfl_sync(kFullMask, incl0, 31);
+        const int n = tot0 + __shfl_sync(kFullMask, incl1, 31);
+        int32_t *oid = ids + (size_t)t * K;
+        float *op = probs ? probs + (size_t)t * K : nullptr;
+        if (n > K) {
+            if (lane < K) {
+                oid[lane] = E;
+                if (op) op[lane] = 0.0f;
+            }
+            continue;
+        }
+        int slot = incl0 - c0;
+        for (unsigned m = m0; m; m &= m - 1) {
+            const int e = 16 * lane + __ffs(m) - 1;
+            oid[slot] = e;
+            if (op) op[slot] = dense ? dense[(size_t)t * E + e] : 0.0f;
+            ++slot;
+        }
+        slot = tot0 + incl1 - c1;
+        for (unsigned m = m1; m; m &= m - 1) {
+            const int e = 16 * (lane + 32) + __ffs(m) - 1;
+            oid[slot] = e;
+            if (op) op[slot] = dense ? dense[(size_t)t * E + e] : 0.0f;
+            ++slot;
+        }
+        if (lane >= n && lane < K) {
+            oid[lane] = -1;
+            if (op) op[lane] = 0.0f;
+        }
+    }
+}
+
 // Compact -> map.  Lane k < K holds the token's slot k; for each expert of its stripe a lane
 // walks the K slots (shuffles, ascending k) and adds the probabilities of the slots naming it.
 __global__ void __launch_bounds__(kRoutingThreads)
@@ -105,6 +172,9 @@ int launch_map_to_topk(const uint8_t *routing_map, const float *dense_probs, int
         (topk_ids && !aligned16(topk_ids)) || (topk_probs && !aligned16(topk_probs)))
         return EP_ERR_INVALID_ARG;
     if (T == 0) return EP_OK;
+    if (E % 16 == 0)   // every map row starts on a 16-byte boundary
+        return launch_pdl(ep_map_to_topk_wide_kernel, dim3(routing_grid(T)), dim3(kRoutingThreads), 0,
+                          st, routing_map, dense_probs, T, E, K, topk_ids, topk_probs);
     return launch_pdl(ep_map_to_topk_kernel, dim3(routing_grid(T)), dim3(kRoutingThreads), 0, st,
                       routing_map, dense_probs, T, E, K, topk_ids, topk_probs);
 }

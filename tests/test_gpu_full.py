@@ -126,3 +126,94 @@ def test_full_size_overflow_then_rerun(ep):
     assert ref.status == oracle.OVERFLOW
     ref = run_full(ep, cfg, C=cfg.rerun_C)
     assert ref.status == 0
+
+
+def test_full_size_fused_call(ep):
+    """ep_dispatch_layout_nvfp4 on the DSv3-like layer, as the benchmark step calls it."""
+    cfg = W.CONFIGS["dsv3"]
+    T, H, E, K, S, P, C = cfg.T, cfg.H, cfg.E, cfg.K, cfg.S, cfg.P, cfg.capacity
+    inp, _ = inputs(cfg)
+    x, ids = inp["x"], inp["topk_ids"]
+    ref = oracle.layout(ids, E, P=P, C=C, S=S)
+    L = new_layout(ep, T, K, E, P, S)
+    out = (torch.full((ref.R_max, H // 2), 0xA5, dtype=torch.uint8, device="cuda"),
+           torch.full((ref.R_max, H // 16), 0xA5, dtype=torch.uint8, device="cuda"),
+           torch.full((ref.R_max,), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16),
+           torch.full((E + S + 1,), -7, dtype=torch.int32, device="cuda"))
+    ep.dispatch_layout_nvfp4(dev(ids), dev_bf16(x), E, P, C, bool(S), out_layout=L, out=out)
+    check_layout(L, ref, ep)
+    toks = sample_tokens(cfg, x, np.random.default_rng(31))
+    check_nvfp4_rows(*out[:3], ref, x, toks, S, E)
+    assert np.array_equal(out[3].cpu().numpy(), ref.row_offsets)
+
+
+def test_full_size_fp8(ep):
+    cfg = W.CONFIGS["dsv3"]
+    T, H, E, K, S, P, C = cfg.T, cfg.H, cfg.E, cfg.K, cfg.S, cfg.P, cfg.capacity
+    inp, _ = inputs(cfg)
+    x, ids = inp["x"], inp["topk_ids"]
+    ref = oracle.layout(ids, E, P=P, C=C, S=S)
+    L = new_layout(ep, T, K, E, P, S)
+    ep.dispatch_layout(dev(ids), E, P, C, bool(S), out=L)
+    codes, scales = ep.dispatch_fp8(dev_bf16(x), L)
+    for t in sample_tokens(cfg, x, np.random.default_rng(32)):
+        c, s = oracle.fp8_quantize_row(x[t])
+        for r in [r for r in ref.row_of[t] if r >= 0] + [ref.row_offsets[E] + t]:
+            assert np.array_equal(codes[r].cpu().numpy(), c), (t, r)
+            assert np.array_equal(scales[r].cpu().numpy().view(np.uint32), s.view(np.uint32)), (t, r)
+
+
+@pytest.mark.parametrize("name,pad,cap", [("dsv3", 128, None), ("dsv3_static", 128, 36864)])
+def test_full_size_padded(ep, name, pad, cap):
+    """Padded layout in full, NVFP4 rows and combine on sampled tokens, every padding row."""
+    cfg = W.CONFIGS[name]
+    T, H, E, K, S, P, C = cfg.T, cfg.H, cfg.E, cfg.K, cfg.S, cfg.P, cfg.capacity
+    inp = W.make_inputs(cfg)
+    x, ids, probs = inp["x"], inp["topk_ids"], inp["probs"]
+    ref = oracle.layout(ids, E, P=P, C=C, S=S, pad_multiple=pad, num_permuted_tokens=cap)
+    assert ref.status == 0
+    L = ep.Layout(T, K, E, P, bool(S), pad_multiple=pad, num_permuted_tokens=cap)
+    ep.dispatch_layout_routed(E, topk_ids=dev(ids), n_parts=P, capacity=C, fused_shared=bool(S),
+                              pad_multiple=pad, num_permuted_tokens=cap, out=L)
+    assert ep.read_status(L) == 0
+    assert np.array_equal(L.row_offsets.cpu().numpy(), ref.row_offsets)
+    assert np.array_equal(L.row_of.cpu().numpy(), ref.row_of)
+    assert np.array_equal(L.expert_ids.cpu().numpy()[:ref.R], ref.expert_ids[:ref.R])
+    assert np.array_equal(L.src_info.cpu().numpy()[:ref.R], ref.src_info[:ref.R])
+    fp4, sc, inv, so = ep.dispatch_nvfp4(dev_bf16(x), L)
+    toks = sample_tokens(cfg, x, np.random.default_rng(33))
+    check_nvfp4_rows(fp4, sc, inv, ref, x, toks, S, E)
+    pad_rows = torch.from_numpy(np.flatnonzero(ref.src_info[:ref.R, 0] < 0)).cuda()
+    if pad_rows.numel():
+        assert (fp4[pad_rows] == 0).all() and (sc[pad_rows] == 0).all()
+        assert (inv.view(torch.int16)[pad_rows] == 0x3F80).all()
+    y_host = np.resize(W.make_expert_out(cfg), (ref.R_max, H)).astype(np.uint16)
+    out = ep.combine(dev_bf16(y_host), dev(probs), L)
+    # each sampled token through a one-token oracle problem, rows mapped into the padded layout
+    got = host_bf16(out)
+    for t in toks:
+        L1 = oracle.layout(ids[t][None, :], E, S=S)
+        src = np.full(L1.R_max, -1, np.int64)
+        for k in range(K):
+            if L1.row_of[0, k] >= 0:
+                src[L1.row_of[0, k]] = ref.row_of[t, k]
+        if S:
+            src[L1.row_offsets[E]] = ref.row_offsets[E] + t
+        y1 = np.zeros((L1.R_max, H), np.uint16)
+        y1[src >= 0] = y_host[src[src >= 0]]
+        _, r64 = oracle.combine(y1, probs[t:t + 1], L1, want64=True)
+        assert_close_bf16(got[t:t + 1], r64, f"token {t}")
+
+
+def test_full_size_routing_map_layout(ep):
+    cfg = W.CONFIGS["dsv3"]
+    T, E, K, S, P, C = cfg.T, cfg.E, cfg.K, cfg.S, cfg.P, cfg.capacity
+    inp, _ = inputs(cfg)
+    m, d = oracle.indices_to_multihot(inp["topk_ids"], inp["probs"], E)
+    rids, rprobs = oracle.routing_map_to_topk(m, d, K)
+    ref = oracle.layout(rids, E, P=P, C=C, S=S)
+    L = new_layout(ep, T, K, E, P, S)
+    _, ids, probs = ep.dispatch_layout_routed(E, routing_map=dev(m), dense_probs=dev(d), K=K,
+                                              n_parts=P, capacity=C, fused_shared=bool(S), out=L)
+    assert np.array_equal(ids.cpu().numpy(), rids) and np.array_equal(probs.cpu().numpy(), rprobs)
+    check_layout(L, ref, ep)

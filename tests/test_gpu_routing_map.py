@@ -19,7 +19,9 @@ def ep():
 
 
 @pytest.mark.parametrize("T,E,K,density", [(1, 1, 1, 1.0), (100, 8, 2, 0.2), (777, 256, 8, 0.03),
-                                           (300, 1000, 32, 0.02), (64, 33, 4, 0.5)])
+                                           (300, 1000, 32, 0.02), (64, 33, 4, 0.5),
+                                           (200, 1024, 32, 0.02), (300, 16, 4, 0.3),
+                                           (129, 128, 8, 0.06), (50, 512, 16, 0.03)])
 def test_map_to_topk(ep, T, E, K, density):
     rng = np.random.default_rng(T + E)
     m = (rng.random((T, E)) < density).astype(np.uint8)
