@@ -444,15 +444,18 @@ ep_layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int 
 // of tokens.  Per CTA:
 //   A. load the range's ids into shared memory (bad ids become -1; with at most 32 partitions a
 //      per-token partition bitmask is built on the way), per-warp expert histograms;
-//   B. one warp per expert group scans the per-warp counts (shuffles), giving each warp's first
-//      local row per expert and the CTA's count per expert; partition token counts from the
-//      bitmasks (one ballot per partition);
-//   C. each CTA pushes its expert counts into every CTA's shared memory, and its partition
-//      counts and bad-id flag into CTA 0's, through distributed shared memory; one cluster
-//      barrier; from then on every read is local: cluster totals -> row_offsets (a block scan),
-//      counts of the CTAs before this one -> this CTA's first row per expert;
-//   D. stable ranks (equal-id lanes by ballots), row_of in flat order, and each routed row staged
-//      in shared memory in expert order, so src_info and expert_ids go out as contiguous runs.
+//   B. one thread per expert walks the 32 per-warp counts, giving each warp's first local row
+//      per expert and the CTA's count per expert; partition token counts from the bitmasks (one
+//      reduction per partition);
+//   C. each CTA pushes its expert counts into every CTA's shared memory (one warp per
+//      destination, 16-byte stores), and its partition counts and bad-id flag into CTA 0's,
+//      through distributed shared memory, then arrives at the cluster barrier.  Before waiting
+//      it does all its local work: its first local position per expert (a block scan), the
+//      stable rank of each routed (t, k) within its expert (equal-id lanes by ballots), and the
+//      staging of each routed row in shared memory in expert order;
+//   D. after the wait every read is local: cluster totals -> row_offsets (a block scan), counts
+//      of the CTAs before this one -> this CTA's first row per expert; then row_of in flat order,
+//      and src_info / expert_ids from the staging area as contiguous runs.
 // One launch, one cluster barrier after start-up, no global scratch, atomics or fences.
 // ---------------------------------------------------------------------------------------
 constexpr int kClThreads = 1024;
@@ -461,7 +464,7 @@ static_assert(kClWarps == 32, "the cluster kernel scans per-warp values with one
 constexpr int kClMaxCtas = 16;            // largest cluster (non-portable; 8 where 16 is refused)
 constexpr int kClMaxIds = 8192;           // ids of one CTA's range held in shared memory
 constexpr int kClIdsPerCta = 2048;        // below this many ids per CTA, use fewer CTAs
-constexpr int kClExpertsPerThread = kMaxE / kClThreads;
+static_assert(kMaxE <= kClThreads, "the cluster kernel gives one thread to each expert");
 constexpr size_t kClMaxSmem = 216 * 1024;   // dynamic; leaves room for the static arrays
 
 // Shared-memory plan of the cluster kernel (ints): per-expert arrays, the pushed counts of every
@@ -507,6 +510,38 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.aligned;" ::: "memory"); }
+
+// Exclusive scan of one value per thread over a 1024-thread block, in thread order: shuffles
+// within each warp, then one warp over the warp totals.  warp_tot holds 32 ints; every thread
+// gets the block total.  Starts and ends with the block in step (two barriers).
+__device__ __forceinline__ int block_exclusive_scan_1024(int v, int *warp_tot, int &total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(kFullMask, incl, o);
+        if (lane >= o) incl += u;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int before = 0;
+    if (warp == 0) {
+        const int w0 = warp_tot[lane];
+        int wi = w0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(kFullMask, wi, o);
+            if (lane >= o) wi += u;
+        }
+        warp_tot[lane] = wi - w0;   // exclusive warp offsets; the total goes in slot 32
+        if (lane == 31) warp_tot[32] = wi;
+    }
+    __syncthreads();
+    before = warp_tot[warp];
+    total = warp_tot[32];
+    return before + incl - v;
+}
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.aligned;" ::: "memory");
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
@@ -525,10 +560,10 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
     int *s_all = smem + m.all, *s_part_all = smem + m.part_all, *s_bad_all = smem + m.bad_all;
     int *s_whist = smem + m.whist, *s_ids = smem + m.ids, *s_stage = smem + m.stage;
     int *s_tokmask = smem + m.tokmask;
-    __shared__ int s_warp[kClWarps];
-    __shared__ int s_warp2[kClWarps];
+    __shared__ int s_warp[kClWarps + 1];    // warp totals of the block scans (+ the block total)
+    __shared__ int s_warp2[kClWarps + 1];
     __shared__ int s_bad;
-    __shared__ int s_routed, s_nvalid;
+    __shared__ int s_nvalid;
 
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
@@ -582,32 +617,22 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
         for (int p = tid; p < P; p += kClThreads) s_part_all[crank * P + p] = 0;   // local scratch row
     __syncthreads();
 
-    // B. per-(warp, expert) exclusive prefix over the warps, and the CTA's count per expert:
-    //    warp w scans experts w, w + 32, ...; lane l holds warp l's count.
-    for (int e0 = warp; e0 < E; e0 += 4 * kClWarps) {   // four independent scans interleaved
-        int c[4], incl[4];
+    // B. per-(warp, expert) exclusive prefix over the 32 warps, and the CTA's count per expert:
+    //    thread e < E walks expert e's per-warp counts, eight independent shared loads at a time.
+    if (tid < E) {
+        int run = 0;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int e = e0 + q * kClWarps;
-            c[q] = e < E ? s_whist[lane * EP + e] : 0;
-            incl[q] = c[q];
-        }
+        for (int h = 0; h < kClWarps; h += 8) {
+            int c[8];
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
+            for (int w = 0; w < 8; ++w) c[w] = s_whist[(h + w) * EP + tid];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int v = __shfl_up_sync(kFullMask, incl[q], o);
-                if (lane >= o) incl[q] += v;
+            for (int w = 0; w < 8; ++w) {
+                s_whist[(h + w) * EP + tid] = run;
+                run += c[w];
             }
         }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int e = e0 + q * kClWarps;
-            if (e < E) {
-                s_whist[lane * EP + e] = incl[q] - c[q];
-                if (lane == 31) s_hist[e] = incl[q];
-            }
-        }
+        s_hist[tid] = run;
     }
     //    tokens per partition: warp w counts partitions w, w + 32, ... from the token masks
     if (masks) {
@@ -622,41 +647,72 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
     }
     __syncthreads();
 
-    // C. push this CTA's counts through distributed shared memory, then one cluster barrier
+    // C. push this CTA's counts through distributed shared memory (warp r writes them into CTA
+    //    r), its partition counts and bad-id flag into CTA 0's, then arrive at the cluster barrier.
     cluster_wait();   // every CTA of the cluster has started
-    for (int idx = tid; idx < ncta * E; idx += kClThreads) {
-        const int r = idx / E, e = idx - r * E;
-        cluster.map_shared_rank(s_all, r)[crank * E + e] = s_hist[e];
+    for (int r = warp; r < ncta; r += kClWarps) {
+        int *dst = cluster.map_shared_rank(s_all, r) + crank * E;
+        if ((E & 3) == 0) {   // 16-byte aligned rows (the plan's offsets are multiples of E)
+            const int4 *src4 = reinterpret_cast<const int4 *>(s_hist);
+            int4 *dst4 = reinterpret_cast<int4 *>(dst);
+            for (int e4 = lane; e4 < E / 4; e4 += 32) dst4[e4] = src4[e4];
+        } else {
+            for (int e = lane; e < E; e += 32) dst[e] = s_hist[e];
+        }
     }
     if (crank != 0) {
         int *rp = cluster.map_shared_rank(s_part_all, 0);
         for (int p = tid; p < P; p += kClThreads) rp[crank * P + p] = s_part_all[crank * P + p];
     }
     if (tid == 0) cluster.map_shared_rank(s_bad_all, 0)[crank] = s_bad;
-    cluster_sync_all();
+    cluster_arrive();   // release: the pushes are visible to every CTA after its wait
 
-    //    cluster totals per expert (thread tid owns experts kClExpertsPerThread*tid + q), and
-    //    their extents: each total padded to the next multiple of pad
-    int mine = 0, mine_local = 0;
-    int before[kClExpertsPerThread], total[kClExpertsPerThread];
-#pragma unroll
-    for (int q = 0; q < kClExpertsPerThread; ++q) {
-        const int e = kClExpertsPerThread * tid + q;
-        before[q] = 0;
-        total[q] = 0;
-        if (e < E) {
-#pragma unroll
-            for (int r = 0; r < kClMaxCtas; ++r) {
-                if (r < ncta) {
-                    const int v = s_all[r * E + e];
-                    if (r < crank) before[q] += v;
-                    total[q] += v;
-                }
-            }
-            mine_local += s_hist[e];
-        }
-        mine += pad > 1 ? (total[q] + pad - 1) / pad * pad : total[q];
+    //    While the other CTAs arrive, everything local: this CTA's first local position per
+    //    expert (an exclusive scan of its counts), the stable rank of every routed (t, k) in its
+    //    expert's local list (equal-id lanes by ballots), and its staging at that expert-major
+    //    local position (flat index in the low bits, expert in the high bits).  s_ids keeps
+    //    (local rank << 10 | expert) for the rows written after the wait.
+    {
+        int tot_l;
+        const int v = tid < E ? s_hist[tid] : 0;
+        const int ex = block_exclusive_scan_1024(v, s_warp2, tot_l);
+        if (tid < E) s_locoff[tid] = ex;
+        if (tid == 0) s_nvalid = tot_l;
     }
+    __syncthreads();
+    {
+        const unsigned lt_mask = (1u << lane) - 1u;
+        for (int base = w0; base < w1; base += 32) {
+            const int i = base + lane;
+            const int id = i < w1 ? s_ids[i] : -1;
+            const unsigned peers = same_key_lanes((unsigned)(id + 1), nbits);
+            int local = -1;
+            if (id >= 0) local = hist[id] + __popc(peers & lt_mask);
+            __syncwarp();
+            if (id >= 0 && lane == __ffs(peers) - 1) hist[id] += __popc(peers);
+            __syncwarp();
+            if (id >= 0) {
+                s_stage[s_locoff[id] + local] = (id << 16) | i;
+                s_ids[i] = (local << 10) | id;
+            }
+        }
+    }
+    cluster_wait();   // acquire: every CTA's counts are in s_all
+
+    //    cluster totals per expert (thread e owns expert e) and their extents: each total padded
+    //    to the next multiple of pad; the counts of the CTAs before this one
+    int before = 0, total = 0;
+    if (tid < E) {
+#pragma unroll
+        for (int r = 0; r < kClMaxCtas; ++r) {
+            if (r < ncta) {
+                const int v = s_all[r * E + tid];
+                if (r < crank) before += v;
+                total += v;
+            }
+        }
+    }
+    const int ext = pad > 1 ? (total + pad - 1) / pad * pad : total;
     //    CTA 0: partition totals against the capacity, and the bad-id flags (status bits kept
     //    above bit 4 of s_bad, whose low bit is this CTA's own bad-id flag)
     if (crank == 0) {
@@ -670,63 +726,18 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
         if (tid < ncta && s_bad_all[tid]) f |= EP_STATUS_BAD_EXPERT;
         if (f) atomicOr(&s_bad, f << 4);
     }
-    //    exclusive scans over experts (thread-major) of the cluster totals and of this CTA's
-    //    counts: within each warp, then one warp over the warp sums
-    int incl = mine, incl_l = mine_local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(kFullMask, incl, o);
-        const int vl = __shfl_up_sync(kFullMask, incl_l, o);
-        if (lane >= o) {
-            incl += v;
-            incl_l += vl;
-        }
-    }
-    if (lane == 31) {
-        s_warp[warp] = incl;
-        s_warp2[warp] = incl_l;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        const int va0 = s_warp[lane], vb0 = s_warp2[lane];
-        int ia = va0, ib = vb0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int va = __shfl_up_sync(kFullMask, ia, o);
-            const int vb = __shfl_up_sync(kFullMask, ib, o);
-            if (lane >= o) {
-                ia += va;
-                ib += vb;
-            }
-        }
-        s_warp[lane] = ia - va0;   // exclusive warp offsets
-        s_warp2[lane] = ib - vb0;
-        if (lane == 31) {
-            s_routed = ia;
-            s_nvalid = ib;
-        }
-    }
-    __syncthreads();
-    const int routed = s_routed, n_valid = s_nvalid;
+    int routed;
+    const int excl = block_exclusive_scan_1024(ext, s_warp, routed);   // ends with a barrier
+    const int n_valid = s_nvalid;
     const int shared_ext = S ? (pad > 1 ? (T + pad - 1) / pad * pad : T) : 0;
-    int excl = s_warp[warp] + incl - mine;
-    int excl_l = s_warp2[warp] + incl_l - mine_local;
-#pragma unroll
-    for (int q = 0; q < kClExpertsPerThread; ++q) {
-        const int e = kClExpertsPerThread * tid + q;
-        const int ext = pad > 1 ? (total[q] + pad - 1) / pad * pad : total[q];
-        if (e < E) {
-            if (crank == 0) row_offsets[e] = excl;
-            s_first[e] = excl + before[q];
-            s_locoff[e] = excl_l;
-            excl_l += s_hist[e];
-            // padding rows of expert e, spread over the cluster's CTAs
-            for (int r = excl + total[q] + crank; r < excl + ext && r < row_limit; r += ncta) {
-                reinterpret_cast<int2 *>(src_info)[r] = make_int2(-1, -1);
-                expert_ids[r] = e;
-            }
+    if (tid < E) {
+        if (crank == 0) row_offsets[tid] = excl;
+        s_first[tid] = excl + before;
+        // padding rows of expert tid, spread over the cluster's CTAs
+        for (int r = excl + total + crank; r < excl + ext && r < row_limit; r += ncta) {
+            reinterpret_cast<int2 *>(src_info)[r] = make_int2(-1, -1);
+            expert_ids[r] = tid;
         }
-        excl += ext;
     }
     if (crank == 0 && tid == 0) {
         int flags = s_bad >> 4;
@@ -737,32 +748,17 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
     }
     __syncthreads();
 
-    // D. stable ranks: row_of in flat order (-1 for a row at or past the row capacity); each
-    //    routed (t, k) staged at its expert-ordered local position (flat index in the low bits,
-    //    expert in the high bits).
-    {
-        const unsigned lt_mask = (1u << lane) - 1u;
-        for (int base = w0; base < w1; base += 32) {
-            const int i = base + lane;
-            const int id = i < w1 ? s_ids[i] : -1;
-            const unsigned peers = same_key_lanes((unsigned)(id + 1), nbits);
-            int local = -1;
-            if (id >= 0) local = hist[id] + __popc(peers & lt_mask);
-            __syncwarp();
-            if (id >= 0 && lane == __ffs(peers) - 1) hist[id] += __popc(peers);
-            __syncwarp();
-            if (i < w1) {
-                int row = -1;
-                if (id >= 0) {
-                    row = s_first[id] + local;
-                    if (row >= row_limit) row = -1;
-                    s_stage[s_locoff[id] + local] = (id << 16) | i;
-                }
-                row_of[(size_t)t0 * K + i] = row;
-            }
+    // D. rows: row_of in flat order (-1 for an unused slot or a row at or past the row
+    //    capacity), then src_info / expert_ids from the staging area in contiguous runs.
+    for (int i = tid; i < n; i += kClThreads) {
+        const int v = s_ids[i];
+        int row = -1;
+        if (v >= 0) {
+            row = s_first[v & 1023] + (v >> 10);
+            if (row >= row_limit) row = -1;
         }
+        row_of[(size_t)t0 * K + i] = row;
     }
-    __syncthreads();
     for (int j = tid; j < n_valid; j += kClThreads) {
         const int v = s_stage[j];
         const int e = v >> 16, i = v & 0xffff;
