@@ -456,6 +456,7 @@ def run_ours(args, cfg):
 
     h2d = sum(t.numel() * t.element_size() for t in (hx, hids, hprobs, hy))
     d2h = sum(t.numel() * t.element_size() for t in ho.values())
+    # serial: every step's copies and kernels one after another on one stream
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize(dev)
@@ -466,11 +467,18 @@ def run_ours(args, cfg):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_t = reduce_max(e0.elapsed_time(e1) * 1e-3, ws, dev)
+    e2e_serial_t = reduce_max(e0.elapsed_time(e1) * 1e-3, ws, dev)
     barrier(ws)
     # the e2e results are the same bytes as the device-resident run
     if not torch.equal(ho["out"].to(dev), out.view(torch.int16)):
         raise RuntimeError("e2e output differs from the device-resident step")
+    del xd16, yd16
+    # pipelined: the same copies and calls for every step, with step i's input copies, step
+    # i-1's kernels and step i-2's output copies in flight together (three streams, two sets of
+    # device buffers)
+    e2e_t = pipelined_e2e(ep, cfg, dev, hx, hids, hprobs, hy, e2e_steps, out)
+    e2e_t = reduce_max(e2e_t, ws, dev)
+    barrier(ws)
 
     if rank != 0:
         if ws > 1:
@@ -521,6 +529,12 @@ def run_ours(args, cfg):
         "static_routing_step": static,
         "e2e": {"value": ws * T * e2e_steps / e2e_t, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "serial_value": ws * T * e2e_steps / e2e_serial_t,
+                "schedule": "pipelined: each step copies its inputs host->device, runs the fused "
+                            "layout + NVFP4 dispatch call and combine, and copies its results "
+                            "device->host; the three overlap across consecutive steps on three "
+                            "streams with two sets of device buffers. serial_value runs the same "
+                            "steps one after another on one stream",
                 "path": "pinned host x/ids/probs/expert outputs -> device, layout + NVFP4 dispatch + "
                         "combine through the C ABI, dispatched rows + metadata + combined output -> host"},
         "gpu_launches": 3 * args.steps,
@@ -537,6 +551,101 @@ def run_ours(args, cfg):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def pipelined_e2e(ep, cfg: W.Config, dev, hx, hids, hprobs, hy, n_steps: int, ref_out,
+                  n_in: int = 1, n_out: int = 1) -> float:
+    """Seconds for n_steps end-to-end steps through the C ABI, pipelined: host->device copies
+    of step i's inputs, step i's fused layout + NVFP4 dispatch and combine, and device->host
+    copies of its dispatched rows, metadata and combined output.  Two sets of device buffers
+    alternate, so step i's copies overlap the kernels of step i-1 and the result copies of step
+    i-2.  The input / result copies can be split by rows over n_in / n_out streams (one
+    cudaMemcpyAsync per slice); on GB300 four input and two result streams measured no faster
+    than one each, the host link being the limit, so one each is the default.  Checks that the
+    last step's host output equals ref_out."""
+    import torch
+    T, H, E, K, S, P, C = cfg.T, cfg.H, cfg.E, cfg.K, cfg.S, cfg.P, cfg.capacity
+    R_max = W.r_max(cfg)
+
+    def slices(n_rows, n):
+        step = (n_rows + n - 1) // n
+        return [(j * step, min(n_rows, (j + 1) * step)) for j in range(n) if j * step < n_rows]
+
+    sets = []
+    for _ in range(2):
+        L = ep.Layout(T, K, E, P, bool(S), device=dev)
+        d = {"x": torch.empty(T, H, dtype=torch.int16, device=dev),
+             "ids": torch.empty(T, K, dtype=torch.int32, device=dev),
+             "probs": torch.empty(T, K, dtype=torch.float32, device=dev),
+             "y": torch.empty(R_max, H, dtype=torch.int16, device=dev),
+             "fp4": torch.empty(R_max, H // 2, dtype=torch.uint8, device=dev),
+             "sc": torch.empty(R_max, H // 16, dtype=torch.uint8, device=dev),
+             "inv": torch.empty(R_max, dtype=torch.int16, device=dev),
+             "so": torch.empty(E + S + 1, dtype=torch.int32, device=dev),
+             "out": torch.empty(T, H, dtype=torch.int16, device=dev), "L": L}
+        d_out = [("fp4", d["fp4"]), ("sc", d["sc"]), ("inv", d["inv"]), ("so", d["so"]), ("out", d["out"]),
+                 ("row_offsets", L.row_offsets), ("expert_ids", L.expert_ids), ("src_info", L.src_info),
+                 ("status", L.status)]
+        host = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in d_out}
+        ev = {"h2d": [torch.cuda.Event() for _ in range(n_in)], "comp": torch.cuda.Event(),
+              "d2h": [torch.cuda.Event() for _ in range(n_out)]}
+        sets.append((d, d_out, host, ev))
+    s_in = [torch.cuda.Stream(dev) for _ in range(n_in)]
+    s_out = [torch.cuda.Stream(dev) for _ in range(n_out)]
+    s_comp = torch.cuda.Stream(dev)
+    big_in = [("x", hx), ("y", hy)]
+    small_in = [("ids", hids), ("probs", hprobs)]
+
+    def one(i):
+        d, d_out, host, ev = sets[i % 2]
+        L = d["L"]
+        for j, s in enumerate(s_in):
+            s.wait_event(ev["comp"])          # step i-2's kernels are done with this set's inputs
+            with torch.cuda.stream(s):
+                for n, h in big_in:
+                    a, b = slices(h.shape[0], n_in)[j]
+                    d[n][a:b].copy_(h[a:b], non_blocking=True)
+                if j == 0:
+                    for n, h in small_in:
+                        d[n].copy_(h, non_blocking=True)
+            ev["h2d"][j].record(s)
+        for e in ev["h2d"]:
+            s_comp.wait_event(e)
+        for e in ev["d2h"]:
+            s_comp.wait_event(e)              # step i-2's results have left this set's outputs
+        ep.dispatch_layout_nvfp4(d["ids"], d["x"].view(torch.bfloat16), E, P, C, bool(S), out_layout=L,
+                                 out=(d["fp4"], d["sc"], d["inv"].view(torch.bfloat16), d["so"]),
+                                 stream=s_comp)
+        ep.combine(d["y"].view(torch.bfloat16), d["probs"], L, out=d["out"].view(torch.bfloat16),
+                   stream=s_comp)
+        ev["comp"].record(s_comp)
+        for j, s in enumerate(s_out):
+            s.wait_event(ev["comp"])
+            with torch.cuda.stream(s):
+                for n, t in d_out:
+                    sl = slices(t.shape[0], n_out)
+                    if j < len(sl):
+                        a, b = sl[j]
+                        host[n][a:b].copy_(t[a:b], non_blocking=True)
+            ev["d2h"][j].record(s)
+
+    for i in range(2):
+        one(i)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in[0])
+    for s in s_in[1:]:
+        s.wait_event(e0)
+    for i in range(n_steps):
+        one(i)
+    for s in s_in + [s_comp] + s_out[1:]:
+        s_out[0].wait_stream(s)
+    e1.record(s_out[0])
+    torch.cuda.synchronize(dev)
+    last = sets[(n_steps - 1) % 2][2]["out"]
+    if not torch.equal(last.to(dev), ref_out.view(torch.int16)):
+        raise RuntimeError("pipelined e2e output differs from the device-resident step")
+    return e0.elapsed_time(e1) * 1e-3
 
 
 def static_routing_step(ep, dev, stream, flush_l2, n_steps: int) -> dict:
