@@ -20,6 +20,8 @@
 //      writes row_of, src_info and expert_ids; it also writes the shared expert's rows.
 #include <cooperative_groups.h>
 
+#include <mutex>
+
 #include "ep_common.cuh"
 #include "ep_host.h"
 
@@ -784,35 +786,42 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
 }
 
 // Largest cluster the device runs for the layout kernel: 16 CTAs where the non-portable size is
-// granted, else 8 (the portable size).  Looked up once per device.
+// granted, else 8 (the portable size); 0 when the kernel cannot get its shared memory (the
+// layout then takes the two-kernel path).  The kernel's attributes are set and the answer looked
+// up once per device, so later calls (and calls inside a stream capture) only launch.
 inline int max_cluster_ctas() {
     constexpr int kMaxDev = 64;
-    static int cached[kMaxDev];
+    static int cached[kMaxDev];   // 0: not looked up; else the answer + 1
+    static std::mutex mu;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 8;
-    if (dev >= 0 && dev < kMaxDev && cached[dev]) return cached[dev];
-    int best = 8;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const bool cacheable = dev >= 0 && dev < kMaxDev;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cacheable && cached[dev]) return cached[dev] - 1;
+    int best = 0;
     if (cudaFuncSetAttribute(ep_layout_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kClMaxSmem) == cudaSuccess &&
-        cudaFuncSetAttribute(ep_layout_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
-                             1) == cudaSuccess) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(16);
-        cfg.blockDim = dim3(kClThreads);
-        cfg.dynamicSmemBytes = kClMaxSmem;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 16;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, ep_layout_cluster_kernel, &cfg) == cudaSuccess && n > 0)
-            best = 16;
+                             (int)kClMaxSmem) == cudaSuccess) {
+        best = 8;
+        if (cudaFuncSetAttribute(ep_layout_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                 1) == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(16);
+            cfg.blockDim = dim3(kClThreads);
+            cfg.dynamicSmemBytes = kClMaxSmem;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 16;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, ep_layout_cluster_kernel, &cfg) == cudaSuccess && n > 0)
+                best = 16;
+        }
     }
     (void)cudaGetLastError();
-    if (dev >= 0 && dev < kMaxDev) cached[dev] = best;
+    if (cacheable) cached[dev] = best + 1;
     return best;
 }
 
@@ -821,16 +830,13 @@ inline int max_cluster_ctas() {
 inline int launch_cluster_layout(const int32_t *ids, int T, int K, int E, int P, int C, int S,
                                  int pad, int row_limit, ep_layout_t *L, cudaStream_t st,
                                  int *ctas_used) {
-    const int ncta = cluster_ctas(T, K, E, P, max_cluster_ctas());
+    const int max_ctas = max_cluster_ctas();
+    if (max_ctas == 0) return -1;   // the two-kernel path needs no shared-memory opt-in
+    const int ncta = cluster_ctas(T, K, E, P, max_ctas);
     if (ncta == 0) return -1;
     *ctas_used = ncta;
     const int tile_t = (T + ncta - 1) / ncta;
     const size_t smem = cluster_smem_bytes(E, P, tile_t, K);
-    if (cudaFuncSetAttribute(ep_layout_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kClMaxSmem) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return -1;   // the two-kernel path needs no such opt-in
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ncta);
     cfg.blockDim = dim3(kClThreads);
@@ -999,7 +1005,6 @@ extern "C" const char *ep_strerror(int code) {
 // when it finishes.  All calls share the one array, so calls whose work overlaps on the GPU
 // (other streams, other threads) race on it.
 // ---------------------------------------------------------------------------------------
-#include <mutex>
 
 namespace ep {
 namespace {
