@@ -429,6 +429,7 @@ def run_ours(args, cfg):
         raise RuntimeError("padded or routing-map layout reported an error on the benchmark workload")
     R_pad = int(Lp.row_offsets[Lp.G].item())
     static = static_routing_step(ep, dev, stream, flush_l2, nb)
+    sweep = config_sweep(ep, dev, stream, flush_l2, min(nb, 100)) if not args.no_sweep else None
 
     # ---- e2e through the public API with pinned host buffers ----
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
@@ -527,6 +528,7 @@ def run_ours(args, cfg):
                          f"{PAD} rows ({R_pad} rows, {R_pad - R} of them padding, written as an "
                          f"all-zero token)"),
         "static_routing_step": static,
+        "configs_sweep": sweep,
         "e2e": {"value": ws * T * e2e_steps / e2e_t, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "serial_value": ws * T * e2e_steps / e2e_serial_t,
@@ -648,6 +650,76 @@ def pipelined_e2e(ep, cfg: W.Config, dev, hx, hids, hprobs, hy, n_steps: int, re
     return e0.elapsed_time(e1) * 1e-3
 
 
+def config_sweep(ep, dev, stream, flush_l2, n_steps: int) -> list:
+    """The benchmark step (fused layout + NVFP4 dispatch call, then combine) on every workload
+    recipe, timed like the headline step (L2 flushed before each step, events around each call).
+    Routing comes from the seeded recipes; x and the expert outputs are seeded device draws
+    (N(0,1) bf16): the kernels' work does not depend on their values.  The large microbatch runs
+    at its rerun capacity, where nothing overflows."""
+    import torch
+    peak, _ = load_peaks()
+    res = []
+    for name, cfg in W.CONFIGS.items():
+        C = cfg.rerun_C if cfg.rerun_C else cfg.capacity
+        T, H, E, K, S, P = cfg.T, cfg.H, cfg.E, cfg.K, cfg.S, cfg.P
+        ids_h, probs_h = W.make_routing(cfg)
+        ids = torch.from_numpy(ids_h).to(dev)
+        probs = torch.from_numpy(probs_h).to(dev)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(9000 + cfg.index)
+        x = torch.randn(T, H, device=dev, generator=gen).to(torch.bfloat16)
+        R_max = W.r_max(cfg)
+        y = torch.randn(R_max, H, device=dev, generator=gen).to(torch.bfloat16)
+        L = ep.Layout(T, K, E, P, bool(S), device=dev)
+        rows = (torch.empty(R_max, H // 2, dtype=torch.uint8, device=dev),
+                torch.empty(R_max, H // 16, dtype=torch.uint8, device=dev),
+                torch.empty(R_max, dtype=torch.bfloat16, device=dev),
+                torch.empty(E + S + 1, dtype=torch.int32, device=dev))
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+
+        def step(evs=None):
+            if evs:
+                evs[0].record(stream)
+            ep.dispatch_layout_nvfp4(ids, x, E, P, C, bool(S), out_layout=L, out=rows, stream=stream)
+            if evs:
+                evs[1].record(stream)
+            ep.combine(y, probs, L, out=out, stream=stream)
+            if evs:
+                evs[2].record(stream)
+
+        step()
+        torch.cuda.synchronize(dev)
+        if ep.read_status(L) != 0:
+            raise RuntimeError(f"layout status on workload {name}")
+        R = int(L.row_offsets[L.G].item())
+        for _ in range(3):
+            flush_l2()
+            step()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_steps)]
+        for e in evs:
+            flush_l2()
+            step(e)
+        torch.cuda.synchronize(dev)
+        t = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[0].elapsed_time(e[2])]
+                      for e in evs]).mean(axis=0) * 1e-3
+        ab = algorithmic_bytes(cfg, R)
+        disp_b, comb_b = ab["layout"] + ab["dispatch_nvfp4"], ab["combine"]
+        res.append({
+            "workload": name, "T": T, "hidden": H, "n_experts": E, "top_k": K, "fused_shared": S,
+            "n_parts": P, "capacity": C, "rows": R, "steps": n_steps,
+            "us": {"dispatch": t[0] * 1e6, "combine": t[1] * 1e6, "step": t[2] * 1e6},
+            "tokens/s": {"dispatch": T / t[0], "combine": T / t[1], "step": T / t[2]},
+            "algorithmic_bytes": {"dispatch": disp_b, "combine": comb_b, "step": disp_b + comb_b},
+            "frac_of_measured_peak": {"dispatch": disp_b / t[0] / 1e9 / peak,
+                                      "combine": comb_b / t[1] / 1e9 / peak,
+                                      "step": (disp_b + comb_b) / t[2] / 1e9 / peak},
+            "frac_of_8TB/s": {"step": (disp_b + comb_b) / t[2] / 8e12},
+        })
+        del x, y, rows, out, L
+        torch.cuda.empty_cache()
+    return res
+
+
 def static_routing_step(ep, dev, stream, flush_l2, n_steps: int) -> dict:
     """Layout + NVFP4 dispatch + combine on the forced-balanced static routing workload, with its
     persisted row count passed as the static row capacity and groups padded to 128 rows; L2
@@ -713,6 +785,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the per-workload sweep (fused layout + NVFP4 dispatch, combine, step)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
