@@ -46,9 +46,10 @@ def check_padded_layout(ep, L, ref):
     assert (ei[n:ref.R_max] == CANARY32).all() and (si[n:ref.R_max] == CANARY32).all()
 
 
-def run_all(ep, cfg, pad, cap, x=None):
-    inp = W.make_inputs(cfg)
-    ids, probs = inp["topk_ids"], inp["probs"]
+def run_all(ep, cfg, pad, cap, x=None, ids=None, probs=None, y=None):
+    inp = W.make_inputs(cfg) if ids is None else None
+    ids = inp["topk_ids"] if ids is None else ids
+    probs = inp["probs"] if probs is None else probs
     x = inp["x"] if x is None else x
     H = x.shape[1]
     ref = oracle.layout(ids, cfg.E, P=cfg.P, C=cfg.capacity, S=cfg.S, pad_multiple=pad,
@@ -85,7 +86,8 @@ def run_all(ep, cfg, pad, cap, x=None):
     if ref.status:
         return ref
     # expert outputs with NaN in every padding row: combine must never read them
-    y = W.make_expert_out(W.scaled(cfg, T=cfg.T))
+    if y is None:
+        y = W.make_expert_out(W.scaled(cfg, T=cfg.T))
     y = np.resize(y, (Rm, H)).astype(np.uint16)
     pad_rows = ref.src_info[:ref.R, 0] < 0
     y[:ref.R][pad_rows] = 0x7FC0
@@ -93,7 +95,7 @@ def run_all(ep, cfg, pad, cap, x=None):
     got = ep.combine(yd, dev(probs), L)
     _, ref64 = oracle.combine(y, probs, ref, want64=True)
     assert_close_bf16(host_bf16(got), ref64, "combine")
-    g = W.make_grad_out(cfg)
+    g = W.bf16_bits_from_f32(np.random.default_rng(cfg.T).standard_normal((cfg.T, H)).astype(np.float32))
     gy = torch.full((Rm, H), -23131, dtype=torch.int16, device="cuda").view(torch.bfloat16)
     gp = torch.full((cfg.T, cfg.K), float("nan"), dtype=torch.float32, device="cuda")
     ep.combine_bwd(dev_bf16(g), yd, dev(probs), L, out=(gy, gp))
@@ -180,3 +182,36 @@ def test_padded_reuse_and_zero_tokens(ep):
     ep.dispatch_layout_routed(8, topk_ids=torch.empty(0, 2, dtype=torch.int32, device="cuda"),
                               fused_shared=True, pad_multiple=4, out=L0)
     assert ep.read_status(L0) == 0 and L0.row_offsets.cpu().tolist() == [0] * 10
+
+
+EDGE = [  # T, K, E, S, P, pad, case
+    (300, 32, 1024, 1, 16, 7, "largest K and E, odd pad"),
+    (129, 1, 1, 0, 1, 3, "one expert, one slot"),
+    (200, 3, 8, 1, 2, 8, "every slot unused"),
+    (257, 4, 3, 1, 1, 5, "duplicate ids"),
+    (17000, 8, 64, 1, 4, 16, "a bad id, two-kernel layout"),
+]
+
+
+@pytest.mark.parametrize("T,K,E,S,P,pad,case", EDGE, ids=[c[-1] for c in EDGE])
+def test_padded_edge_cases(ep, T, K, E, S, P, pad, case):
+    rng = np.random.default_rng(T + K + E)
+    H = 256 if T < 10000 else 128
+    if case == "duplicate ids":
+        ids = rng.integers(0, E, size=(T, K)).astype(np.int32)
+    elif case == "every slot unused":
+        ids = np.full((T, K), -1, np.int32)
+    else:
+        ids = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+        ids[rng.random((T, K)) < 0.05] = -1
+    if case.startswith("a bad id"):
+        ids[5, 3] = E
+    x = W.bf16_bits_from_f32(rng.standard_normal((T, H)).astype(np.float32))
+    p = rng.random((T, K)).astype(np.float32)
+    y = W.bf16_bits_from_f32(rng.standard_normal((T * K + T, H)).astype(np.float32))
+    cfg = W.Config(900, "edge", T=T, H=H, E=E, K=K, S=S, P=P)
+    ref = run_all(ep, cfg, pad, None, x=x, ids=ids, probs=p, y=y)
+    if case.startswith("a bad id"):
+        assert ref.status == oracle.BAD_EXPERT
+    else:
+        assert ref.status == 0
