@@ -200,6 +200,23 @@ def oracle_step(oracle, cfg: W.Config, inp: dict, y: np.ndarray, T_s: int) -> No
     oracle.combine(y[:L.R_max], inp["probs"][:T_s], L)
 
 
+def host_cpu() -> dict:
+    """The host the oracle runs on: its logical CPU count and model name (from lscpu when it is
+    there, else the platform string)."""
+    import platform
+    import subprocess
+    model = platform.processor() or platform.machine()
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    return {"host_cpus": os.cpu_count(), "host_cpu_model": model}
+
+
 def time_oracle(cfg: W.Config, inp: dict, y: np.ndarray, budget_s: float, T_s: int | None = None):
     import oracle
     oracle.build()
@@ -250,7 +267,8 @@ def run_reference(args, cfg):
             "steps": steps, "warmup": warm, "ms_per_step": dt / steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32/f64", "data": "synthetic",
             "config": workload_config(cfg),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
+                             **host_cpu()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -547,7 +565,8 @@ def run_ours(args, cfg):
         v, T_s, reps, secs = time_oracle(cfg, inp, y_host, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": f"first {T_s} of {T} tokens per step (layout over them, NVFP4 "
-                                          f"dispatch, combine), {reps} step(s), {secs:.1f} s, single thread"}
+                                          f"dispatch, combine), {reps} step(s), {secs:.1f} s, single thread",
+                                **host_cpu()}
     print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist
