@@ -132,16 +132,21 @@ def test_layout_reuse_across_calls(ep):
         check_layout(L, oracle.layout(ids, E, P=P, C=C, S=S), ep)
 
 
-FUSED_CASES = [("tiny", None, None), ("dsv3", 900, None), ("qwen3", 1500, None),
-               ("dsv3", 7000, 7000),            # more tokens per CTA than staging slots: rounds
-               ("dsv3_large", 1000, 610)]       # capacity overflow: nothing written
+FUSED_CASES = [("tiny", None, None, None), ("dsv3", 900, None, None), ("qwen3", 1500, None, None),
+               ("dsv3", 7000, 7000, None),      # more tokens per CTA than staging slots: rounds
+               ("dsv3_large", 1000, 610, None),  # capacity overflow: nothing written
+               ("mixtral", 3000, None, 784),    # H not a multiple of 256: the per-token kernel
+               ("mixtral", 90000, None, 256)]   # beyond two rounds per CTA: the per-token kernel
 
 
-@pytest.mark.parametrize("name,T,C", FUSED_CASES, ids=[f"{c[0]}-{c[1]}" for c in FUSED_CASES])
-def test_fused_layout_nvfp4(ep, name, T, C):
+@pytest.mark.parametrize("name,T,C,H", FUSED_CASES,
+                         ids=[f"{c[0]}-{c[1]}" + (f"-H{c[3]}" if c[3] else "") for c in FUSED_CASES])
+def test_fused_layout_nvfp4(ep, name, T, C, H):
     """ep_dispatch_layout_nvfp4 gives exactly the layout and NVFP4 rows of the two calls."""
     cfg = W.CONFIGS[name]
     kw = {"C": C} if C is not None else {}
+    if H is not None:
+        kw["H"] = H
     cfg = W.scaled(cfg, T=T, **kw) if (T or kw) else cfg
     inp = W.make_inputs(cfg)
     x, ids = inp["x"], inp["topk_ids"]
