@@ -152,6 +152,8 @@ ep_dispatch_nvfp4_kernel(const uint16_t *__restrict__ x, int T, int H, int K, in
     }
 }
 
+constexpr int kBf16Chunks = 4;   // 16-byte chunks of a row one thread holds at a time
+
 __global__ void __launch_bounds__(256)
 ep_dispatch_bf16_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int E, int S, int R_max,
                         int nfill, int pad, const int32_t *__restrict__ row_of,
@@ -173,11 +175,24 @@ ep_dispatch_bf16_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int
     __syncthreads();
     const int nv = H / 8;
     const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
-    for (int c = tid; c < nv; c += blockDim.x) {
-        const uint4 d = ld_stream(src + c);
+    // the row's 16-byte chunks of this thread are all requested before the first is stored
+    // (up to kBf16Chunks per thread at a time)
+    for (int c0 = tid; c0 < nv; c0 += kBf16Chunks * blockDim.x) {
+        uint4 d[kBf16Chunks];
+#pragma unroll
+        for (int i = 0; i < kBf16Chunks; ++i) {
+            const int c = c0 + i * blockDim.x;
+            if (c < nv) d[i] = ld_stream(src + c);
+        }
         for (int k = 0; k < nrows; ++k) {
             const int r = s_rows[k];
-            if (r >= 0 && r < R_max) st_stream(out + (size_t)r * H + (size_t)c * 8, d);
+            if (r < 0 || r >= R_max) continue;
+            uint16_t *dst = out + (size_t)r * H;
+#pragma unroll
+            for (int i = 0; i < kBf16Chunks; ++i) {
+                const int c = c0 + i * blockDim.x;
+                if (c < nv) st_stream(dst + (size_t)c * 8, d[i]);
+            }
         }
     }
 }
