@@ -8,9 +8,11 @@
 
 namespace ep {
 
-// One buffer whose padding rows a kernel fills: `row_bytes` per row (even), every 32-bit word
-// of a padding row set to `pattern` (16-bit periodic when row_bytes % 4 != 0).  A null ptr
-// means no buffer.
+// One buffer whose padding rows a kernel fills: `row_bytes` per row, every 32-bit word of a
+// padding row set to `pattern`.  Rows are written with the widest store their size and start
+// allow: 16-, 4-, 2- or 1-byte stores, so a pattern must be 16-bit periodic when row_bytes is
+// not a multiple of 4, and byte periodic when it is odd (the NVFP4 block-scale row, H/16 bytes,
+// can be odd).  A null ptr means no buffer.
 struct PadFill {
     void *ptr;
     int row_bytes;
@@ -25,9 +27,11 @@ __device__ __forceinline__ void fill_row(const PadFill &f, int row, int lane) {
         for (int i = lane; i < f.row_bytes / 16; i += 32) st_stream(reinterpret_cast<uint4 *>(p) + i, v);
     } else if (f.row_bytes % 4 == 0) {
         for (int i = lane; i < f.row_bytes / 4; i += 32) reinterpret_cast<uint32_t *>(p)[i] = f.pattern;
-    } else {
+    } else if (f.row_bytes % 2 == 0) {
         for (int i = lane; i < f.row_bytes / 2; i += 32)
             reinterpret_cast<uint16_t *>(p)[i] = (uint16_t)f.pattern;
+    } else {   // odd row size: rows start on any byte
+        for (int i = lane; i < f.row_bytes; i += 32) p[i] = (unsigned char)f.pattern;
     }
 }
 

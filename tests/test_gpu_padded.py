@@ -119,6 +119,8 @@ CASES = [  # name, T, H, pad, capacity mode
     ("dsv3", 600, 1024, 128, "exact"),
     ("mixtral", 1500, 512, 8, "exact"),
     ("dsv3_large", 2000, 512, 32, None),
+    ("tiny", 300, 48, 4, None),                 # 3-byte block-scale rows (odd)
+    ("qwen3", 400, 272, 16, "exact"),           # 17-byte block-scale rows (odd)
 ]
 
 
