@@ -115,3 +115,48 @@ def test_random_case(ep, seed):
     gx = ep.dispatch_bwd(yd, L)
     _, rgx64 = oracle.dispatch_bwd(y, ref, want64=True)
     assert_close_bf16(host_bf16(gx), rgx64, "grad_input")
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_fused_call_and_routing_map(ep, seed):
+    """The fused layout + NVFP4 call, and the layout of the same routing given as a dense map,
+    on seeded random shapes (no padding: the fused call takes none)."""
+    c = draw_case(100 + seed)
+    T, K, E, P, S, H, C = (c[k] for k in ("T", "K", "E", "P", "S", "H", "C"))
+    ids, x, probs = c["ids"], c["x"], c["probs"]
+    if T == 0:
+        return
+    ref = oracle.layout(ids, E, P=P, C=C, S=S)
+    L = ep.Layout(T, K, E, P, bool(S))
+    L.expert_ids.fill_(CANARY32)
+    L.src_info.fill_(CANARY32)
+    Rm = ref.R_max
+    out = (torch.full((Rm, H // 2), 0xA5, dtype=torch.uint8, device="cuda"),
+           torch.full((Rm, H // 16), 0xA5, dtype=torch.uint8, device="cuda"),
+           torch.full((Rm,), -23131, dtype=torch.int16, device="cuda").view(torch.bfloat16),
+           torch.full((E + S + 1,), -7, dtype=torch.int32, device="cuda"))
+    ep.dispatch_layout_nvfp4(dev(ids), dev_bf16(x), E, P, C, bool(S), out_layout=L, out=out)
+    assert ep.read_status(L) == ref.status
+    assert np.array_equal(L.row_offsets.cpu().numpy(), ref.row_offsets)
+    assert np.array_equal(L.row_of.cpu().numpy(), ref.row_of)
+    assert np.array_equal(L.src_info.cpu().numpy()[:ref.R], ref.src_info[:ref.R])
+    rfp4, rsc, rinv, _ = oracle.dispatch_nvfp4(x, ref, fill=0xA5)
+    assert np.array_equal(out[0].cpu().numpy(), rfp4)
+    assert np.array_equal(out[1].cpu().numpy(), rsc)
+    assert np.array_equal(host_bf16(out[2]), rinv)
+
+    # the same routing as a dense map (a map holds each expert once per token)
+    m, d = oracle.indices_to_multihot(ids, probs, E)
+    rids, rprobs = oracle.routing_map_to_topk(m, d, K)
+    ref2 = oracle.layout(rids, E, P=P, C=C, S=S)
+    L2 = ep.Layout(T, K, E, P, bool(S))
+    _, gids, gprobs = ep.dispatch_layout_routed(E, routing_map=dev(m), dense_probs=dev(d), K=K,
+                                                n_parts=P, capacity=C, fused_shared=bool(S), out=L2)
+    assert np.array_equal(gids.cpu().numpy(), rids)
+    assert np.array_equal(gprobs.cpu().numpy(), rprobs)
+    assert ep.read_status(L2) == ref2.status
+    assert np.array_equal(L2.row_offsets.cpu().numpy(), ref2.row_offsets)
+    assert np.array_equal(L2.row_of.cpu().numpy(), ref2.row_of)
+    gm, gd = ep.indices_to_multihot(dev(ids), dev(probs), E)
+    assert np.array_equal(gm.cpu().numpy(), m)
+    assert np.array_equal(gd.cpu().numpy().view(np.uint32), d.view(np.uint32))
