@@ -49,7 +49,7 @@ def draw_case(seed):
                 rng=rng)
 
 
-@pytest.mark.parametrize("seed", range(24))
+@pytest.mark.parametrize("seed", range(48))
 def test_random_case(ep, seed):
     c = draw_case(seed)
     T, K, E, P, S, H, pad, C, cap = (c[k] for k in ("T", "K", "E", "P", "S", "H", "pad", "C", "cap"))
@@ -117,7 +117,7 @@ def test_random_case(ep, seed):
     assert_close_bf16(host_bf16(gx), rgx64, "grad_input")
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(24))
 def test_random_fused_call_and_routing_map(ep, seed):
     """The fused layout + NVFP4 call, and the layout of the same routing given as a dense map,
     on seeded random shapes (no padding: the fused call takes none)."""
