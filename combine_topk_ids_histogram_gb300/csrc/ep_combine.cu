@@ -108,7 +108,7 @@ template <int KMAX>
 __global__ void __launch_bounds__(kCombineThreads)
 ep_combine_bwd_kernel(const uint16_t *__restrict__ g, const uint16_t *__restrict__ y,
                       const float *__restrict__ probs, int T, int H, int K, int E, int S, int R_max,
-                      int nfill, int pad, const int32_t *__restrict__ row_of,
+                      int nfill, int fparts, int pad, const int32_t *__restrict__ row_of,
                       const int32_t *__restrict__ row_offsets, const int32_t *__restrict__ src_info,
                       const int32_t *__restrict__ status, uint16_t *__restrict__ grad_y,
                       float *__restrict__ grad_p) {
@@ -118,8 +118,8 @@ ep_combine_bwd_kernel(const uint16_t *__restrict__ g, const uint16_t *__restrict
     pdl_begin();
     if (load_status(status)) return;
     if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: zero gradient rows
-        fill_group_padding(blockIdx.x, pad, row_offsets, src_info, PadFill{grad_y, 2 * H, 0u},
-                           PadFill{nullptr, 0, 0u}, PadFill{nullptr, 0, 0u});
+        fill_group_padding(blockIdx.x / fparts, blockIdx.x % fparts, fparts, pad, row_offsets, src_info,
+                           PadFill{grad_y, 2 * H, 0u}, PadFill{nullptr, 0, 0u}, PadFill{nullptr, 0, 0u});
         return;
     }
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -250,11 +250,12 @@ extern "C" int ep_combine_bwd(const uint16_t *grad_out, const uint16_t *expert_o
     cudaStream_t st = as_stream(stream);
     const int K = L->K;
     const int R_max = layout_rows(L);
-    const int nfill = fill_ctas(L);   // padding rows of a padded layout get a zero gradient
+    const int nfill = fill_ctas(L, kCombineThreads);   // padding rows get a zero gradient
+    const int fparts = fill_parts(L, kCombineThreads);
 #define EP_BWD_CASE(KM)                                                                        \
     return launch_pdl(ep_combine_bwd_kernel<KM>, dim3(L->T + nfill), dim3(kCombineThreads), 0, st, \
                       grad_out, expert_out, probs, L->T, H, K, L->E, L->fused_shared, R_max,   \
-                      nfill, L->pad_multiple, (const int32_t *)L->row_of,                      \
+                      nfill, fparts, L->pad_multiple, (const int32_t *)L->row_of,              \
                       (const int32_t *)L->row_offsets, (const int32_t *)L->src_info,           \
                       (const int32_t *)L->status, grad_expert_out, grad_probs)
     if (K <= 2) EP_BWD_CASE(2);

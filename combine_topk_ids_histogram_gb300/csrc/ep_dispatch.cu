@@ -54,7 +54,7 @@ __device__ __forceinline__ float absmax8(uint4 v) {
 template <int BPT, int MAXT, int MINB>
 __global__ void __launch_bounds__(MAXT, MINB)
 ep_dispatch_nvfp4_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int E, int S, int G, int R_max,
-                         int early, int nfill, int pad,
+                         int early, int nfill, int fparts, int pad,
                          const int32_t *__restrict__ row_of, const int32_t *__restrict__ row_offsets,
                          const int32_t *__restrict__ src_info,
                          const int32_t *__restrict__ status, uint8_t *__restrict__ out_fp4,
@@ -68,8 +68,10 @@ ep_dispatch_nvfp4_kernel(const uint16_t *__restrict__ x, int T, int H, int K, in
     //             only once every earlier kernel had completed), so x is read and quantised
     //             while the layout still runs, and the layout's outputs are read after the wait.
     if (!early) pdl_begin();
-    if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: one group's padding rows
-        if (!load_status(status)) fill_group_padding_call(blockIdx.x, pad, row_offsets, src_info, f0, f1, f2);
+    if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: a group's padding rows
+        if (!load_status(status))
+            fill_group_padding_call(blockIdx.x / fparts, blockIdx.x % fparts, fparts, pad, row_offsets,
+                                    src_info, f0, f1, f2);
         return;
     }
     const int tid = threadIdx.x;
@@ -156,15 +158,15 @@ constexpr int kBf16Chunks = 4;   // 16-byte chunks of a row one thread holds at 
 
 __global__ void __launch_bounds__(256)
 ep_dispatch_bf16_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int E, int S, int R_max,
-                        int nfill, int pad, const int32_t *__restrict__ row_of,
+                        int nfill, int fparts, int pad, const int32_t *__restrict__ row_of,
                         const int32_t *__restrict__ row_offsets, const int32_t *__restrict__ src_info,
                         const int32_t *__restrict__ status, uint16_t *__restrict__ out, PadFill f0) {
     __shared__ int s_rows[kMaxRowsPerToken];
     pdl_begin();
     if (load_status(status)) return;
-    if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: one group's padding rows
-        fill_group_padding_call(blockIdx.x, pad, row_offsets, src_info, f0, PadFill{nullptr, 0, 0u},
-                           PadFill{nullptr, 0, 0u});
+    if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: a group's padding rows
+        fill_group_padding_call(blockIdx.x / fparts, blockIdx.x % fparts, fparts, pad, row_offsets,
+                                src_info, f0, PadFill{nullptr, 0, 0u}, PadFill{nullptr, 0, 0u});
         return;
     }
     const int tid = threadIdx.x;
@@ -211,15 +213,16 @@ constexpr int kFp8Block = 128;
 template <int MAXT, int MINB>
 __global__ void __launch_bounds__(MAXT, MINB)
 ep_dispatch_fp8_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int E, int S, int R_max,
-                       int nfill, int pad, const int32_t *__restrict__ row_of,
+                       int nfill, int fparts, int pad, const int32_t *__restrict__ row_of,
                        const int32_t *__restrict__ row_offsets, const int32_t *__restrict__ src_info,
                        const int32_t *__restrict__ status, uint8_t *__restrict__ out_fp8,
                        float *__restrict__ out_scales, PadFill f0, PadFill f1) {
     __shared__ int s_rows[kMaxRowsPerToken];
     pdl_begin();
-    if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: one group's padding rows
+    if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: a group's padding rows
         if (!load_status(status))
-            fill_group_padding_call(blockIdx.x, pad, row_offsets, src_info, f0, f1, PadFill{nullptr, 0, 0u});
+            fill_group_padding_call(blockIdx.x / fparts, blockIdx.x % fparts, fparts, pad, row_offsets,
+                                    src_info, f0, f1, PadFill{nullptr, 0, 0u});
         return;
     }
     const int tid = threadIdx.x;
@@ -471,11 +474,6 @@ namespace {
 int launch_nvfp4(const uint16_t *input_tokens, int H, const ep_layout_t *L, uint8_t *out_fp4,
                  uint8_t *out_scales, uint16_t *out_rowwise_inv_scale, int32_t *scales_offsets,
                  int early, cudaStream_t st) {
-    // padding rows (padded layouts; the fused call's layout is never padded): codes 0, block
-    // scales 0, inverse global scale bf16(1/1) = 0x3F80 -- the dispatch of an all-zero token
-    const int nfill = early ? 0 : fill_ctas(L);
-    const PadFill f0{out_fp4, H / 2, 0u}, f1{out_scales, H / 16, 0u},
-        f2{out_rowwise_inv_scale, 2, 0x3F803F80u};
     if (!layout_ok(L) || !hidden_ok(H)) return EP_ERR_INVALID_ARG;
     const int bpt = (H % 32 == 0) ? 2 : 1;
     const int nth = H / (16 * bpt);
@@ -488,6 +486,12 @@ int launch_nvfp4(const uint16_t *input_tokens, int H, const ep_layout_t *L, uint
         if (p && !aligned16(p)) return EP_ERR_INVALID_ARG;
     // enough threads to load the K (+1 shared) row indices of the token
     const int threads = max((nth + 31) / 32 * 32, (L->K + 1 + 31) / 32 * 32);
+    // padding rows (padded layouts; the fused call's layout is never padded): codes 0, block
+    // scales 0, inverse global scale bf16(1/1) = 0x3F80 -- the dispatch of an all-zero token
+    const int nfill = early ? 0 : fill_ctas(L, threads);
+    const int fparts = fill_parts(L, threads);
+    const PadFill f0{out_fp4, H / 2, 0u}, f1{out_scales, H / 16, 0u},
+        f2{out_rowwise_inv_scale, 2, 0x3F803F80u};
     const int grid = (L->T > 0 ? L->T : 1) + nfill;
     const int G = L->E + L->fused_shared;
     const int R_max = layout_rows(L);
@@ -496,8 +500,8 @@ int launch_nvfp4(const uint16_t *input_tokens, int H, const ep_layout_t *L, uint
 #define EP_NVFP4_LAUNCH(BPT, MAXT, MINB)                                                        \
     return launch_pdl(ep_dispatch_nvfp4_kernel<BPT, MAXT, MINB>, dim3(grid), dim3(threads), 0, st, \
                       input_tokens, L->T, H, L->K, L->E, L->fused_shared, G, R_max, early, nfill, \
-                      L->pad_multiple, row_of, row_offsets, src_info, status, out_fp4, out_scales, \
-                      out_rowwise_inv_scale, scales_offsets, f0, f1, f2)
+                      fparts, L->pad_multiple, row_of, row_offsets, src_info, status, out_fp4,   \
+                      out_scales, out_rowwise_inv_scale, scales_offsets, f0, f1, f2)
     // Up to 256 threads (H <= 8192): 5 such CTAs per SM without spilling.
     if (bpt == 2 && threads <= 256) EP_NVFP4_LAUNCH(2, 256, 5);
     if (bpt == 2) EP_NVFP4_LAUNCH(2, 1024, 1);
@@ -553,12 +557,12 @@ extern "C" int ep_dispatch_bf16(const uint16_t *input_tokens, int hidden_size, c
     if (L->T > 0 && (!input_tokens || !out)) return EP_ERR_INVALID_ARG;
     if ((input_tokens && !aligned16(input_tokens)) || (out && !aligned16(out))) return EP_ERR_INVALID_ARG;
     if (L->T == 0) return EP_OK;
-    const int nfill = fill_ctas(L);   // padding rows: zeros
+    const int nfill = fill_ctas(L, 256);   // padding rows: zeros
     return launch_pdl(ep_dispatch_bf16_kernel, dim3(L->T + nfill), dim3(256), 0, as_stream(stream),
                       input_tokens, L->T, H, L->K, L->E, L->fused_shared, layout_rows(L), nfill,
-                      L->pad_multiple, (const int32_t *)L->row_of, (const int32_t *)L->row_offsets,
-                      (const int32_t *)L->src_info, (const int32_t *)L->status, out,
-                      PadFill{out, 2 * H, 0u});
+                      fill_parts(L, 256), L->pad_multiple, (const int32_t *)L->row_of,
+                      (const int32_t *)L->row_offsets, (const int32_t *)L->src_info,
+                      (const int32_t *)L->status, out, PadFill{out, 2 * H, 0u});
 }
 
 extern "C" int ep_dispatch_fp8(const uint16_t *input_tokens, int hidden_size, const ep_layout_t *L,
@@ -573,17 +577,18 @@ extern "C" int ep_dispatch_fp8(const uint16_t *input_tokens, int hidden_size, co
     cudaStream_t st = as_stream(stream);
     const int threads = max(H / 32, 32 * ((L->K + 1 + 31) / 32));   // H % 128 == 0: whole warps
     const int R_max = layout_rows(L);
-    const int nfill = fill_ctas(L);
+    const int nfill = fill_ctas(L, threads);
+    const int fparts = fill_parts(L, threads);
     // padding rows: codes 0 and the scale of an all-zero block, 1.0f
     const PadFill f0{out_fp8, H, 0u}, f1{out_scales, 4 * (H / kFp8Block), 0x3F800000u};
     if (threads <= 256)
         return launch_pdl(ep_dispatch_fp8_kernel<256, 5>, dim3(L->T + nfill), dim3(threads), 0, st,
-                          input_tokens, L->T, H, L->K, L->E, L->fused_shared, R_max, nfill,
+                          input_tokens, L->T, H, L->K, L->E, L->fused_shared, R_max, nfill, fparts,
                           L->pad_multiple, (const int32_t *)L->row_of, (const int32_t *)L->row_offsets,
                           (const int32_t *)L->src_info, (const int32_t *)L->status, out_fp8,
                           out_scales, f0, f1);
     return launch_pdl(ep_dispatch_fp8_kernel<1024, 1>, dim3(L->T + nfill), dim3(threads), 0, st,
-                      input_tokens, L->T, H, L->K, L->E, L->fused_shared, R_max, nfill,
+                      input_tokens, L->T, H, L->K, L->E, L->fused_shared, R_max, nfill, fparts,
                       L->pad_multiple, (const int32_t *)L->row_of, (const int32_t *)L->row_offsets,
                       (const int32_t *)L->src_info, (const int32_t *)L->status, out_fp8, out_scales,
                       f0, f1);

@@ -37,10 +37,12 @@ __device__ __forceinline__ void fill_row(const PadFill &f, int row, int lane) {
 
 // Group g's padding rows close the group: [first, row_offsets[g+1]), at most pad - 1 of them,
 // where `first` is the lowest row among the group's last pad - 1 rows whose source token is -1
-// (every row before it is one of the group's routed rows).  The whole CTA finds `first`, then
-// its warps write the rows.  Call only while the layout's status word is 0 (then every row is
-// below R_max).
-__device__ __forceinline__ void fill_group_padding(int g, int pad, const int32_t *__restrict__ row_offsets,
+// (every row before it is one of the group's routed rows).  The group's rows are shared by
+// `nparts` CTAs: the whole CTA finds `first`, then its warps write the rows of part `part`
+// (every nparts-th warp-sized step).  Call only while the layout's status word is 0 (then every
+// row is below R_max).
+__device__ __forceinline__ void fill_group_padding(int g, int part, int nparts, int pad,
+                                                   const int32_t *__restrict__ row_offsets,
                                                    const int32_t *__restrict__ src_info, const PadFill &f0,
                                                    const PadFill &f1, const PadFill &f2) {
     __shared__ int s_first;
@@ -52,7 +54,7 @@ __device__ __forceinline__ void fill_group_padding(int g, int pad, const int32_t
         if (src_info[2 * (size_t)r] < 0) atomicMin(&s_first, r);
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    for (int r = s_first + warp; r < hi; r += nw) {
+    for (int r = s_first + part * nw + warp; r < hi; r += nw * nparts) {
         fill_row(f0, r, lane);
         fill_row(f1, r, lane);
         fill_row(f2, r, lane);
@@ -61,13 +63,26 @@ __device__ __forceinline__ void fill_group_padding(int g, int pad, const int32_t
 
 // The same as a separate function, for kernels whose own register allocation should not
 // carry the fill's.
-static __device__ __noinline__ void fill_group_padding_call(int g, int pad, const int32_t *__restrict__ row_offsets,
-                                                     const int32_t *__restrict__ src_info, PadFill f0,
-                                                     PadFill f1, PadFill f2) {
-    fill_group_padding(g, pad, row_offsets, src_info, f0, f1, f2);
+static __device__ __noinline__ void fill_group_padding_call(int g, int part, int nparts, int pad,
+                                                            const int32_t *__restrict__ row_offsets,
+                                                            const int32_t *__restrict__ src_info,
+                                                            PadFill f0, PadFill f1, PadFill f2) {
+    fill_group_padding(g, part, nparts, pad, row_offsets, src_info, f0, f1, f2);
 }
 
-// Extra leading CTAs of a grid for a layout's padding rows: one per group when padded.
-inline int fill_ctas(const ep_layout_t *L) { return L->pad_multiple > 1 ? L->E + L->fused_shared : 0; }
+// CTAs sharing one group's padding rows, for CTAs of `threads` threads: enough for about eight
+// warps per group (a group has at most pad - 1 padding rows, and a lone warp's stores drain
+// slowly while the token CTAs keep the memory system busy).
+inline int fill_parts(const ep_layout_t *L, int threads) {
+    const int warps = threads / 32 > 0 ? threads / 32 : 1;
+    int parts = (8 + warps - 1) / warps;
+    if (parts > L->pad_multiple - 1) parts = L->pad_multiple - 1;
+    return parts > 1 ? parts : 1;
+}
+
+// Extra leading CTAs of a grid for a layout's padding rows: fill_parts per group when padded.
+inline int fill_ctas(const ep_layout_t *L, int threads) {
+    return L->pad_multiple > 1 ? (L->E + L->fused_shared) * fill_parts(L, threads) : 0;
+}
 
 }  // namespace ep
