@@ -100,6 +100,28 @@ def test_largest_k_and_e(ep):
     full_check(ep, ids, x, p, y, 1024, P=16, S=1)
 
 
+def test_largest_k_and_e_two_kernel_layout(ep):
+    """K = 32 and E = 1024 with more ids (160,000) than one thread-block cluster holds, so the
+    two-kernel layout runs at its widest count table."""
+    ids, x, p, y = rand_case(5000, 32, 1024, 32, 17, unused=0.05)
+    full_check(ep, ids, x, p, y, 1024, P=8, S=1)
+
+
+def test_largest_token_count(ep):
+    """T at the limit the entry points accept (2^24 tokens, 50,331,648 rows with the shared
+    copies): every grid and every row index at the top of its range.  Ids include -1 and
+    repeats within a token."""
+    T, K, E, H = 1 << 24, 2, 8, 16
+    rng = np.random.default_rng(16)
+    ids = rng.integers(-1, E, size=(T, K), dtype=np.int32)
+    x = W.bf16_bits_from_f32(rng.standard_normal((T, H), dtype=np.float32))
+    p = rng.random((T, K), dtype=np.float32)
+    y = np.resize(W.bf16_bits_from_f32(rng.standard_normal((65537, H), dtype=np.float32)),
+                  (T * K + T, H))
+    ref = full_check(ep, ids, x, p, y, E, P=4, S=1)
+    assert ref.status == 0 and ref.R > T
+
+
 def test_single_expert_single_slot(ep):
     ids, x, p, y = rand_case(129, 1, 1, 32, 8)
     full_check(ep, ids, x, p, y, 1)

@@ -188,6 +188,7 @@ def test_padded_reuse_and_zero_tokens(ep):
 
 EDGE = [  # T, K, E, S, P, pad, case
     (300, 32, 1024, 1, 16, 7, "largest K and E, odd pad"),
+    (100, 2, 4, 1, 2, 65536, "largest pad multiple"),
     (129, 1, 1, 0, 1, 3, "one expert, one slot"),
     (200, 3, 8, 1, 2, 8, "every slot unused"),
     (257, 4, 3, 1, 1, 5, "duplicate ids"),
