@@ -86,12 +86,41 @@ __device__ __forceinline__ float e4m3_value(uint32_t c) {
 }
 
 // ---------------------------------------------------------------------------------------
-// Block-wide maximum of non-negative floats (all threads get the result).  `red` holds one
-// slot per warp.
+// Largest magnitude of packed bf16 values, without unpacking.  With the sign bit cleared, the
+// 15-bit pattern of a finite bf16 orders like its magnitude (subnormals included), so two
+// 16-bit unsigned maxima per instruction give the exact maximum.  (Infinity compares above
+// every finite value; a NaN, outside the method's domain, would compare above infinity.)
 // ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+// Per 16-bit half: the largest magnitude pattern among the word's halves at that position.
+__device__ __forceinline__ uint32_t absmax_bits(uint4 v) {
+    constexpr uint32_t kMag = 0x7fff7fffu;
+    return max_u16x2(max_u16x2(v.x & kMag, v.y & kMag), max_u16x2(v.z & kMag, v.w & kMag));
+}
+// The larger of the two halves, as an fp32 value (exact: bf16 -> fp32 is a shift).
+__device__ __forceinline__ float absmax_value(uint32_t m) {
+    return __uint_as_float(max_u16x2(m, m >> 16) << 16);
+}
+// max |x| over the 16 bf16 values of two 16-byte words.
+__device__ __forceinline__ float absmax16(uint4 a, uint4 b) {
+    return absmax_value(max_u16x2(absmax_bits(a), absmax_bits(b)));
+}
+
+// ---------------------------------------------------------------------------------------
+// Block-wide maximum of non-negative floats (all threads get the result).  `red` holds one
+// slot per warp.  Non-negative floats order like their bit patterns, so each warp reduces
+// with one unsigned-maximum instruction.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ float warp_max_nonneg(float v) {
+    return __uint_as_float(__reduce_max_sync(kFullMask, __float_as_uint(v)));
+}
+
 __device__ __forceinline__ float block_max_nonneg(float v, float *red) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, o));
+    v = warp_max_nonneg(v);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (lane == 0) red[warp] = v;
     __syncthreads();

@@ -42,15 +42,6 @@ __device__ __forceinline__ uint2 quant_block(uint4 a, uint4 b, float bmax, float
     return make_uint2(lo, hi);
 }
 
-__device__ __forceinline__ float absmax8(uint4 v) {
-    float f[8];
-    unpack8(v, f);
-    float m = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
-    return m;
-}
-
 template <int BPT, int MAXT, int MINB>
 __global__ void __launch_bounds__(MAXT, MINB)
 ep_dispatch_nvfp4_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int E, int S, int G, int R_max,
@@ -96,7 +87,7 @@ ep_dispatch_nvfp4_kernel(const uint16_t *__restrict__ x, int T, int H, int K, in
     float tmax = 0.0f;
 #pragma unroll
     for (int b = 0; b < BPT; ++b) {
-        bmax[b] = fmaxf(absmax8(v[2 * b]), absmax8(v[2 * b + 1]));
+        bmax[b] = absmax16(v[2 * b], v[2 * b + 1]);
         tmax = fmaxf(tmax, bmax[b]);
     }
     // Row maximum (exact) -> global scale g = 2688 / a (1 for an all-zero row).
@@ -242,7 +233,8 @@ ep_dispatch_fp8_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int 
     else if (tid == K && S) my_row = row_offsets[E] + t;
     if (load_status(status)) return;
     if (tid < K + S) s_rows[tid] = my_row;
-    float m = fmaxf(fmaxf(absmax8(v[0]), absmax8(v[1])), fmaxf(absmax8(v[2]), absmax8(v[3])));
+    float m = absmax_value(max_u16x2(max_u16x2(absmax_bits(v[0]), absmax_bits(v[1])),
+                                     max_u16x2(absmax_bits(v[2]), absmax_bits(v[3]))));
     m = fmaxf(m, __shfl_xor_sync(kFullMask, m, 1));   // the four threads of the block
     m = fmaxf(m, __shfl_xor_sync(kFullMask, m, 2));
     __syncthreads();
@@ -308,7 +300,7 @@ constexpr int kStageMaxThreads = 256;
 
 __global__ void __launch_bounds__(kStageMaxThreads, 4)
 ep_dispatch_nvfp4_staged_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int E, int S, int G,
-                                int R_max, int tpc, int early, const int32_t *__restrict__ row_of,
+                                int R_max, int early, const int32_t *__restrict__ row_of,
                                 const int32_t *__restrict__ row_offsets,
                                 const int32_t *__restrict__ status, uint8_t *__restrict__ out_fp4,
                                 uint8_t *__restrict__ out_scales, uint16_t *__restrict__ out_inv,
@@ -323,7 +315,10 @@ ep_dispatch_nvfp4_staged_kernel(const uint16_t *__restrict__ x, int T, int H, in
     const unsigned slot_bytes = code_bytes + scale_bytes;   // a multiple of 16
     unsigned char *s_stage = smem_raw;                    // [kStageSlots][slot_bytes]
     uint16_t *s_inv = reinterpret_cast<uint16_t *>(smem_raw + (size_t)kStageSlots * slot_bytes);
-    const int tb = blockIdx.x * tpc, te = min(T, tb + tpc);
+    // Token ranges of ceil(T / grid) or floor(T / grid) tokens: every SM gets the same number
+    // of CTAs and each CTA within one token of the same work.
+    const int tb = (int)((long long)blockIdx.x * T / gridDim.x);
+    const int te = (int)((long long)(blockIdx.x + 1) * T / gridDim.x);
     bool waited = false;
     if (!early) {
         pdl_begin();
@@ -348,11 +343,9 @@ ep_dispatch_nvfp4_staged_kernel(const uint16_t *__restrict__ x, int T, int H, in
 #pragma unroll
                 for (int i = 0; i < 4; ++i) vn[i] = ld_stream(src + i);
             }
-            const float b0 = fmaxf(absmax8(v[0]), absmax8(v[1]));
-            const float b1 = fmaxf(absmax8(v[2]), absmax8(v[3]));
-            float m = fmaxf(b0, b1);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFullMask, m, o));
+            const float b0 = absmax16(v[0], v[1]);
+            const float b1 = absmax16(v[2], v[3]);
+            const float m = warp_max_nonneg(fmaxf(b0, b1));
             if (lane == 0) s_red[par][warp] = m;
             __syncthreads();
             float a = 0.0f;
@@ -432,17 +425,17 @@ inline int launch_nvfp4_staged(const uint16_t *x, int H, const ep_layout_t *L, u
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > busy_sms)
         grid = grid / sms * (sms - busy_sms);   // only the SMs the layout leaves free
     if (grid <= 0) return -1;
-    const int tpc = (T + grid - 1) / grid;
+    if (grid > T) grid = T;
+    const int tpc = (T + grid - 1) / grid;   // the most tokens a CTA gets
     // Beyond two rounds of staging slots per CTA the rounds alternate reading and writing inside
     // each CTA, and the per-token kernel (in early mode) is faster: on GB300, 54 tokens per CTA
     // (32,768 tokens at H = 7168) took 304 us staged against 274 us per token, while 16 tokens
     // per CTA (16,384 at H = 4096) took 41 us staged against 48 us.
     if (tpc > 2 * kStageSlots) return -1;
-    grid = (T + tpc - 1) / tpc;
     const int G = L->E + L->fused_shared;
     const int R_max = layout_rows(L);
     return launch_pdl(ep_dispatch_nvfp4_staged_kernel, dim3(grid), dim3(threads), smem, st, x, T, H,
-                      L->K, L->E, L->fused_shared, G, R_max, tpc, early, (const int32_t *)L->row_of,
+                      L->K, L->E, L->fused_shared, G, R_max, early, (const int32_t *)L->row_of,
                       (const int32_t *)L->row_offsets, (const int32_t *)L->status, out_fp4, out_scales,
                       out_inv, scales_offsets);
 }

@@ -181,6 +181,42 @@ def test_rows_with_zeros_subnormals_and_outliers(ep):
     full_check(ep, ids, x, p, y, E)
 
 
+@pytest.mark.parametrize("H", [256, 512])
+def test_fused_call_rows_with_zeros_subnormals_and_outliers(ep, H):
+    """The same special rows through the fused layout + NVFP4 call, whose staged kernel (H a
+    multiple of 256) takes the row and block maxima on packed bf16 patterns."""
+    T, K, E = 600, 3, 16
+    ids, x, p, y = rand_case(T, K, E, H, 14)
+    x[3] = 0
+    x[4] = 0x8000
+    x[5, :] = 0
+    x[5, 7] = 0x0001
+    x[5, H - 3] = 0x8002
+    x[6] = W.bf16_bits_from_f32(W.f32_from_bf16_bits(x[6]) * np.float32(7.5e37))
+    x[7] = W.bf16_bits_from_f32(W.f32_from_bf16_bits(x[7]) * np.float32(1e-36))
+    x[8, ::16] = 0
+    x[9, 16:32] = 0x0003
+    x[10, 32:48] = 0x807F                               # largest negative subnormal block
+    x[11] = W.bf16_bits_from_f32(-np.abs(W.f32_from_bf16_bits(x[11])))   # all negative
+    x[12, :] = 0x0001
+    x[12, 200] = 0x7F7F                                 # largest finite bf16 beside subnormals
+    assert np.isfinite(W.f32_from_bf16_bits(x)).all()
+    ref = oracle.layout(ids, E, P=4, C=T, S=1)
+    L = new_layout(ep, T, K, E, 4, 1)
+    R_max = ref.R_max
+    out = (torch.full((R_max, H // 2), 0x5A, dtype=torch.uint8, device="cuda"),
+           torch.full((R_max, H // 16), 0x5A, dtype=torch.uint8, device="cuda"),
+           torch.full((R_max,), 0x1357, dtype=torch.int16, device="cuda").view(torch.bfloat16),
+           torch.full((E + 2,), -7, dtype=torch.int32, device="cuda"))
+    ep.dispatch_layout_nvfp4(dev(ids), dev_bf16(x), E, 4, T, True, out_layout=L, out=out)
+    check_layout(L, ref, ep)
+    rfp4, rsc, rinv, rso = oracle.dispatch_nvfp4(x, ref, fill=0x5A)
+    assert np.array_equal(out[0].cpu().numpy(), rfp4)
+    assert np.array_equal(out[1].cpu().numpy(), rsc)
+    assert np.array_equal(host_bf16(out[2])[:ref.R], rinv[:ref.R])
+    assert np.array_equal(out[3].cpu().numpy(), rso)
+
+
 def test_status_word_and_read_status(ep):
     ids = dev(np.array([[0, 1], [2, 99]], np.int32))
     L = ep.dispatch_layout(ids, 4, n_parts=2)
