@@ -1,4 +1,6 @@
-// ep_common.cuh -- device helpers shared by the dispatch / combine kernels (sm_103a).
+// ep_common.cuh -- device helpers shared by the dispatch / combine kernels (sm_103a): streaming
+// 16-byte accesses, programmatic dependent launch, the status word and bf16 <-> fp32.  The
+// quantisation helpers of the dispatch kernels are in ep_quant.cuh.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -56,78 +58,6 @@ __device__ __forceinline__ void unpack8(uint4 v, float f[8]) {
 __device__ __forceinline__ uint4 pack8(const float f[8]) {
     return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
                       pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
-}
-
-// ---------------------------------------------------------------------------------------
-// NVFP4 element and scale formats, converted by the sm_100-family hardware instructions
-// (round to nearest even, saturating to the largest finite value).
-// ---------------------------------------------------------------------------------------
-// Two fp32 -> two E2M1 codes in one byte: `lo` in bits 0-3, `hi` in bits 4-7.
-__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
-    uint32_t r;
-    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
-        : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-// Two fp32 -> two E4M3 codes: `lo` in bits 0-7, `hi` in bits 8-15.
-__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
-    unsigned short r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-// Value of a non-negative finite E4M3 code (bias 7; exponent field 0 is subnormal, m * 2^-9).
-// Built bit by bit, so it is exact.
-__device__ __forceinline__ float e4m3_value(uint32_t c) {
-    uint32_t ex = (c >> 3) & 15u, m = c & 7u;
-    if (ex == 0) return (float)m * 0.001953125f;   // m * 2^-9, exact
-    return __uint_as_float(((ex + 120u) << 23) | (m << 20));
-}
-
-// ---------------------------------------------------------------------------------------
-// Largest magnitude of packed bf16 values, without unpacking.  With the sign bit cleared, the
-// 15-bit pattern of a finite bf16 orders like its magnitude (subnormals included), so two
-// 16-bit unsigned maxima per instruction give the exact maximum.  (Infinity compares above
-// every finite value; a NaN, outside the method's domain, would compare above infinity.)
-// ---------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-// Per 16-bit half: the largest magnitude pattern among the word's halves at that position.
-__device__ __forceinline__ uint32_t absmax_bits(uint4 v) {
-    constexpr uint32_t kMag = 0x7fff7fffu;
-    return max_u16x2(max_u16x2(v.x & kMag, v.y & kMag), max_u16x2(v.z & kMag, v.w & kMag));
-}
-// The larger of the two halves, as an fp32 value (exact: bf16 -> fp32 is a shift).
-__device__ __forceinline__ float absmax_value(uint32_t m) {
-    return __uint_as_float(max_u16x2(m, m >> 16) << 16);
-}
-// max |x| over the 16 bf16 values of two 16-byte words.
-__device__ __forceinline__ float absmax16(uint4 a, uint4 b) {
-    return absmax_value(max_u16x2(absmax_bits(a), absmax_bits(b)));
-}
-
-// ---------------------------------------------------------------------------------------
-// Block-wide maximum of non-negative floats (all threads get the result).  `red` holds one
-// slot per warp.  Non-negative floats order like their bit patterns, so each warp reduces
-// with one unsigned-maximum instruction.
-// ---------------------------------------------------------------------------------------
-__device__ __forceinline__ float warp_max_nonneg(float v) {
-    return __uint_as_float(__reduce_max_sync(kFullMask, __float_as_uint(v)));
-}
-
-__device__ __forceinline__ float block_max_nonneg(float v, float *red) {
-    v = warp_max_nonneg(v);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    const int nw = (blockDim.x + 31) >> 5;
-    float m = 0.0f;
-    for (int w = 0; w < nw; ++w) m = fmaxf(m, red[w]);
-    return m;
 }
 
 }  // namespace ep

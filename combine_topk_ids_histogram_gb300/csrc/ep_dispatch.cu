@@ -14,6 +14,7 @@
 #include "ep_async.cuh"
 #include "ep_host.h"
 #include "ep_padding.cuh"
+#include "ep_quant.cuh"
 
 namespace ep {
 namespace {
@@ -35,7 +36,9 @@ __device__ __forceinline__ uint2 quant_block(uint4 a, uint4 b, float bmax, float
     uint32_t lo = 0, hi = 0;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-        const uint32_t byte = cvt_e2m1x2(__fmul_rn(bf16_lo(w[q]), r), __fmul_rn(bf16_hi(w[q]), r));
+        float p0, p1;
+        mul2_rn(bf16_lo(w[q]), bf16_hi(w[q]), r, p0, p1);
+        const uint32_t byte = cvt_e2m1x2(p0, p1);
         if (q < 4) lo |= byte << (8 * q);
         else hi |= byte << (8 * (q - 4));
     }
@@ -249,10 +252,10 @@ ep_dispatch_fp8_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int 
     uint32_t c[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-        const uint32_t lo = cvt_e4m3x2(__fmul_rn(bf16_lo(w[2 * q]), sc), __fmul_rn(bf16_hi(w[2 * q]), sc));
-        const uint32_t hi =
-            cvt_e4m3x2(__fmul_rn(bf16_lo(w[2 * q + 1]), sc), __fmul_rn(bf16_hi(w[2 * q + 1]), sc));
-        c[q] = lo | (hi << 16);
+        float p0, p1, p2, p3;
+        mul2_rn(bf16_lo(w[2 * q]), bf16_hi(w[2 * q]), sc, p0, p1);
+        mul2_rn(bf16_lo(w[2 * q + 1]), bf16_hi(w[2 * q + 1]), sc, p2, p3);
+        c[q] = cvt_e4m3x2(p0, p1) | (cvt_e4m3x2(p2, p3) << 16);
     }
     // Lane l holds bytes [32l, 32l + 32) of its warp's 1 KiB of codes.  After the exchange, lane l
     // holds bytes [16l, 16l + 16) (w1) and [512 + 16l, 512 + 16l + 16) (w2): the 16-byte half
@@ -306,9 +309,13 @@ ep_dispatch_nvfp4_staged_kernel(const uint16_t *__restrict__ x, int T, int H, in
                                 uint8_t *__restrict__ out_scales, uint16_t *__restrict__ out_inv,
                                 int32_t *__restrict__ scales_offsets) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    __shared__ float s_red[2][kStageMaxThreads / 32];
+    __shared__ __align__(16) float s_red[2][kStageMaxThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = blockDim.x >> 5;
+    // The slots of absent warps (which no warp writes) hold 0, so every step reads all eight
+    // with two 16-byte loads; the first step's barrier orders these stores before the reads.
+    static_assert(kStageMaxThreads / 32 == 8, "two float4 per reduction step");
+    if (tid < 16 && (tid & 7) >= nwarps) s_red[tid >> 3][tid & 7] = 0.0f;
     const int nth = H / 32;
     const bool active = tid < nth;
     const unsigned code_bytes = (unsigned)H / 2, scale_bytes = (unsigned)H / 16;
@@ -348,8 +355,10 @@ ep_dispatch_nvfp4_staged_kernel(const uint16_t *__restrict__ x, int T, int H, in
             const float m = warp_max_nonneg(fmaxf(b0, b1));
             if (lane == 0) s_red[par][warp] = m;
             __syncthreads();
-            float a = 0.0f;
-            for (int w = 0; w < nwarps; ++w) a = fmaxf(a, s_red[par][w]);
+            const float4 r0 = reinterpret_cast<const float4 *>(s_red[par])[0];
+            const float4 r1 = reinterpret_cast<const float4 *>(s_red[par])[1];
+            const float a = fmaxf(fmaxf(fmaxf(r0.x, r0.y), fmaxf(r0.z, r0.w)),
+                                  fmaxf(fmaxf(r1.x, r1.y), fmaxf(r1.z, r1.w)));
             float g = 1.0f;
             if (a != 0.0f) {
                 g = __fdiv_rn(2688.0f, a);

@@ -217,6 +217,58 @@ def test_fused_call_rows_with_zeros_subnormals_and_outliers(ep, H):
     assert np.array_equal(out[3].cpu().numpy(), rso)
 
 
+def _every_scale_code_rows(T, rng):
+    """Rows of 128 blocks (H = 2048) whose block scales take every finite E4M3 code.  Element
+    0 of each row is 2688, so g = 2688 / 2688 = 1 and sf = blockmax / 6; block c (c = 1..126)
+    has the maximum 6 * value(c), so sf is exactly the value of code c, and the other 15
+    elements are random fractions of that maximum.  Block 127 is all zero (code 0)."""
+    H = 2048
+    codes = np.arange(1, 127)
+    vals = np.array([oracle.e4m3_decode(int(c)) for c in codes], np.float64)
+    x = np.zeros((T, H), np.float32)
+    for t in range(T):
+        perm = rng.permutation(126)                       # which block gets which code
+        for b in range(126):
+            bm = 6.0 * vals[perm[b]]
+            blk = bm * rng.uniform(-1, 1, 16)
+            blk[rng.integers(16)] = bm * (1 if rng.random() < 0.5 else -1)
+            x[t, 16 * b:16 * b + 16] = blk
+        x[t, 126 * 16:127 * 16] = 0
+        x[t, 127 * 16:] = 0
+        x[t, 126 * 16] = 2688.0                           # the row maximum (block 126: code 0x7E)
+    bits = W.bf16_bits_from_f32(x)
+    # the block maxima and 2688 are bf16 values, so rounding to bf16 keeps them
+    assert np.abs(W.f32_from_bf16_bits(bits)).max() == 2688.0
+    return bits
+
+
+def test_every_block_scale_code(ep):
+    """Every E4M3 block-scale code (and with it every g / s quotient of the element scaling)
+    through both NVFP4 kernels: the per-token dispatch and the fused call's staged one."""
+    T, K, E = 300, 2, 8
+    rng = np.random.default_rng(21)
+    x = _every_scale_code_rows(T, rng)
+    ids, _, p, y = rand_case(T, K, E, 16, 22)
+    ref = oracle.layout(ids, E, P=1, C=T, S=1)
+    rfp4, rsc, rinv, rso = oracle.dispatch_nvfp4(x, ref, fill=0x5A)
+    assert set(np.unique(rsc[:ref.R])) >= set(range(0, 127)), "the rows cover every code"
+    for fused in (False, True):
+        L = new_layout(ep, T, K, E, 1, 1)
+        out = (torch.full((ref.R_max, 1024), 0x5A, dtype=torch.uint8, device="cuda"),
+               torch.full((ref.R_max, 128), 0x5A, dtype=torch.uint8, device="cuda"),
+               torch.full((ref.R_max,), 0x1357, dtype=torch.int16, device="cuda").view(torch.bfloat16),
+               torch.full((E + 2,), -7, dtype=torch.int32, device="cuda"))
+        if fused:
+            ep.dispatch_layout_nvfp4(dev(ids), dev_bf16(x), E, 1, T, True, out_layout=L, out=out)
+        else:
+            ep.dispatch_layout(dev(ids), E, 1, T, True, out=L)
+            ep.dispatch_nvfp4(dev_bf16(x), L, out=out)
+        check_layout(L, ref, ep)
+        assert np.array_equal(out[0].cpu().numpy(), rfp4), f"codes (fused={fused})"
+        assert np.array_equal(out[1].cpu().numpy(), rsc), f"scales (fused={fused})"
+        assert np.array_equal(host_bf16(out[2])[:ref.R], rinv[:ref.R])
+
+
 def test_status_word_and_read_status(ep):
     ids = dev(np.array([[0, 1], [2, 99]], np.int32))
     L = ep.dispatch_layout(ids, 4, n_parts=2)
