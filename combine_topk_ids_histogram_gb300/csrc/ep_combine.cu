@@ -9,9 +9,12 @@
 // gradients combined back per token).
 //
 // Combine runs as many CTAs as fit on the GPU at once, each looping over tokens.  A thread owns
-// 8-element (16-byte) column slices of the token; for a slice it issues the loads of all of
-// the token's K (+1 shared) rows before accumulating, so up to K+1 independent 16-byte loads
-// per thread are in flight, and it already holds the next token's row indices.  The
+// column slices of the token, two adjacent 16-byte words (16 elements) at a time for K <= 8
+// (one word for wider K, whose rows would not fit in registers); for a slice it issues the
+// loads of all of the token's K (+1 shared) rows before accumulating, so up to 2(K+1)
+// independent 16-byte loads per thread are in flight, and it already holds the next token's
+// row indices.  With two words per thread a 128-thread CTA reads 4 KB of each row per step:
+// on GB300 that beat 2 KB steps by 3.6% (94.5 against 98.0 us for the DSv3-shaped combine).  The
 // accumulation is fp32 with one fused multiply-add per term, in ascending slot order with the
 // shared row last, which makes the result deterministic.  The backward kernel keeps one CTA
 // per token.
@@ -27,8 +30,12 @@ constexpr int kCombineThreads = 128;
 // Persistent: a CTA loops over tokens t = blockIdx.x, blockIdx.x + gridDim.x, ...  While it
 // streams token t's rows it already holds the row indices and weights of its next token, so a
 // token starts with its row loads, never with a metadata round trip.
+// Resident CTAs per SM the register budget is sized for.
+template <int KMAX>
+constexpr int combine_min_blocks() { return KMAX <= 2 ? 8 : KMAX <= 4 ? 6 : KMAX <= 8 ? 4 : 1; }
+
 template <int KMAX, bool WEIGHTED>
-__global__ void __launch_bounds__(kCombineThreads, KMAX <= 8 ? 9 : 1)
+__global__ void __launch_bounds__(kCombineThreads, combine_min_blocks<KMAX>())
 ep_combine_kernel(const uint16_t *__restrict__ y, const float *__restrict__ probs, int T, int H, int K,
                   int E, int S, int R_max, const int32_t *__restrict__ row_of,
                   const int32_t *__restrict__ row_offsets, const int32_t *__restrict__ status,
@@ -74,27 +81,38 @@ ep_combine_kernel(const uint16_t *__restrict__ y, const float *__restrict__ prob
         // rather than held in registers, which keeps enough CTAs resident per SM.
         const int *rows = s_rows[buf];
         const float *w = s_w[buf];
-        for (int c = tid; c < nv; c += blockDim.x) {
-            uint4 d[KMAX + 1];
+        // VW adjacent words per step (H % 16 == 0, so nv is even)
+        constexpr int VW = KMAX <= 8 ? 2 : 1;
+        for (int c = VW * tid; c < nv; c += VW * blockDim.x) {
+            uint4 d[VW][KMAX + 1];
 #pragma unroll
             for (int k = 0; k <= KMAX; ++k) {
                 const int r = rows[k];
-                if (r >= 0) d[k] = ld_stream(y + (size_t)r * H + (size_t)c * 8);
-            }
-            float acc[8];
+                if (r >= 0) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+                    for (int j = 0; j < VW; ++j) d[j][k] = ld_stream(y + (size_t)r * H + (size_t)(c + j) * 8);
+                }
+            }
+            float acc[VW][8];
+#pragma unroll
+            for (int j = 0; j < VW; ++j)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[j][i] = 0.0f;
 #pragma unroll
             for (int k = 0; k <= KMAX; ++k) {
                 if (rows[k] >= 0) {
                     const float wk = w[k];
-                    float f[8];
-                    unpack8(d[k], f);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[i] = fmaf(wk, f[i], acc[i]);
+                    for (int j = 0; j < VW; ++j) {
+                        float f[8];
+                        unpack8(d[j][k], f);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[j][i] = fmaf(wk, f[i], acc[j][i]);
+                    }
                 }
             }
-            st_stream(out + (size_t)t * H + (size_t)c * 8, pack8(acc));
+#pragma unroll
+            for (int j = 0; j < VW; ++j) st_stream(out + (size_t)t * H + (size_t)(c + j) * 8, pack8(acc[j]));
         }
         if (tid <= KMAX) {
             s_rows[buf ^ 1][tid] = r_next;
