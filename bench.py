@@ -315,27 +315,29 @@ def run_ours(args, cfg):
         flush.fill_(1)
         torch.amax(flush_rd, dim=0, out=flush_sink)
 
-    def step(evs=None, per_kernel=False):
+    def step(evs=(None, None, None, None), per_kernel=False):
         """One step: ep_dispatch_layout_nvfp4 (layout and NVFP4 dispatch in one call, the
-        quantisation overlapping the layout) then ep_combine.  Timed steps record an event at
-        the start, between dispatch and combine (so the dominant kernel, combine, is timed on
-        its own stream) and at the end.  The per-kernel breakdown loop instead calls
-        ep_dispatch_layout and ep_dispatch_nvfp4 separately, with an event between them."""
-        if evs:
-            evs[0].record(stream)
+        quantisation overlapping the layout) then ep_combine.  evs holds the events to record:
+        at the start, after the layout (per-kernel loop only), between dispatch and combine, and
+        at the end (None: not recorded).  The timed steps record only the first and the last:
+        an event recorded between two kernels holds the GPU idle for a few microseconds before
+        the next one starts.  A second pass with an event between dispatch and combine times
+        combine, the dominant kernel, on its own stream.  The per-kernel breakdown loop instead
+        calls ep_dispatch_layout and ep_dispatch_nvfp4 separately, with events between them."""
+        def rec(i):
+            if evs[i] is not None:
+                evs[i].record(stream)
+        rec(0)
         if per_kernel:
             ep.dispatch_layout(ids, E, P, C, bool(S), out=L, stream=stream)
-            if evs:
-                evs[1].record(stream)
+            rec(1)
             ep.dispatch_nvfp4(x, L, out=(fp4, sc, inv, so), stream=stream)
         else:
             ep.dispatch_layout_nvfp4(ids, x, E, P, C, bool(S), out_layout=L, out=(fp4, sc, inv, so),
                                      stream=stream)
-        if evs:
-            evs[2].record(stream)
+        rec(2)
         ep.combine(y, probs, L, out=out, stream=stream)
-        if evs:
-            evs[3].record(stream)
+        rec(3)
 
     # correctness of the run itself: no overflow, every row in use
     step()
@@ -357,7 +359,9 @@ def run_ours(args, cfg):
         pass
     sampler = ClockSampler(uuid) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+    evs = [(ev(), None, None, ev()) for _ in range(args.steps)]
     barrier(ws)
     torch.cuda.synchronize(dev)
     t_host0 = time.time()
@@ -368,17 +372,25 @@ def run_ours(args, cfg):
     barrier(ws)
     t_host1 = time.time()
     clocks = sampler.stop(t_host0, t_host1) if sampler else None
-
-    per = np.array([[e[2].elapsed_time(e[3]), e[0].elapsed_time(e[3]), e[0].elapsed_time(e[2])]
-                    for e in evs]) * 1e-3  # s: combine, step, fused layout + dispatch
-    total = float(per[:, 1].sum())
+    per_step = np.array([e[0].elapsed_time(e[3]) for e in evs]) * 1e-3   # s
+    total = float(per_step.sum())
     total_max = reduce_max(total, ws, dev)
     value = ws * T * args.steps / total_max
+
+    # the same steps again with an event between the two calls: combine (the dominant kernel)
+    # and the fused call timed live on their stream
+    evm = [(ev(), None, ev(), ev()) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush_l2()
+        step(evm[i])
+    torch.cuda.synchronize(dev)
+    per = np.array([[e[2].elapsed_time(e[3]), e[0].elapsed_time(e[3]), e[0].elapsed_time(e[2])]
+                    for e in evm]) * 1e-3  # s: combine, step with the middle event, fused call
     comb_s = float(per[:, 0].mean())
 
     # per-kernel breakdown (diagnostic, after the timed region): an event between every kernel
     nb = min(args.steps, 200)
-    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nb)]
+    evb = [(ev(), ev(), ev(), ev()) for _ in range(nb)]
     for i in range(nb):
         flush_l2()
         step(evb[i], per_kernel=True)
@@ -517,6 +529,13 @@ def run_ours(args, cfg):
     times.update(extra)
     ab["layout+dispatch_nvfp4 (fused call)"] = ab["layout"] + ab["dispatch_nvfp4"]
     times["layout+dispatch_nvfp4 (fused call)"] = float(per[:, 2].mean())
+    step_timing = {
+        "us_per_step": total / args.steps * 1e6,
+        "us_per_step_with_middle_event": float(per[:, 1].mean()) * 1e6,
+        "note": ("the timed steps record an event at each step's start and end only; the second "
+                 "pass records one more between the fused call and combine, which times both but "
+                 "holds the GPU idle for a few microseconds before combine starts"),
+    }
     for name, sec in times.items():
         gbs = ab[name] / sec / 1e9
         kernels[name] = {"us": sec * 1e6, "algorithmic_bytes": ab[name], "GB/s": gbs,
@@ -535,10 +554,12 @@ def run_ours(args, cfg):
         "step_roofline": {"algorithmic_bytes": step_bytes, "achieved_GB/s": step_bytes / step_s / 1e9,
                           "frac_of_measured_peak": step_bytes / step_s / 1e9 / peak,
                           "frac_of_8TB/s": step_bytes / step_s / 8e12},
+        "step_timing": step_timing,
         "kernels": kernels,
         "kernels_note": (f"layout, dispatch_nvfp4 and combine: mean of {nb} diagnostic steps after the "
                          "timed region that call ep_dispatch_layout and ep_dispatch_nvfp4 separately, "
-                         "events between kernels; the fused call from the timed steps; the other "
+                         "events between kernels; the fused call from the second pass of the step "
+                         "(an event between the fused call and combine); the other "
                          "entries (not in the step) timed alone on the same routing, L2 flushed before "
                          f"each call: dispatch_bf16, combine_bwd, dispatch_bwd, dispatch_fp8, the layout "
                          f"from the routing as a dense map (map -> ids, then the layout), "
@@ -671,7 +692,8 @@ def pipelined_e2e(ep, cfg: W.Config, dev, hx, hids, hprobs, hy, n_steps: int, re
 
 def config_sweep(ep, dev, stream, flush_l2, n_steps: int) -> list:
     """The benchmark step (fused layout + NVFP4 dispatch call, then combine) on every workload
-    recipe, timed like the headline step (L2 flushed before each step, events around each call).
+    recipe, timed like the headline step: L2 flushed before each step; the step timed with an
+    event at its start and end, then the two calls timed in a second pass with an event between.
     Routing comes from the seeded recipes; x and the expert outputs are seeded device draws
     (N(0,1) bf16): the kernels' work does not depend on their values.  The large microbatch runs
     at its rerun capacity, where nothing overflows."""
@@ -696,14 +718,14 @@ def config_sweep(ep, dev, stream, flush_l2, n_steps: int) -> list:
                 torch.empty(E + S + 1, dtype=torch.int32, device=dev))
         out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
 
-        def step(evs=None):
-            if evs:
+        def step(evs=(None, None, None)):
+            if evs[0] is not None:
                 evs[0].record(stream)
             ep.dispatch_layout_nvfp4(ids, x, E, P, C, bool(S), out_layout=L, out=rows, stream=stream)
-            if evs:
+            if evs[1] is not None:
                 evs[1].record(stream)
             ep.combine(y, probs, L, out=out, stream=stream)
-            if evs:
+            if evs[2] is not None:
                 evs[2].record(stream)
 
         step()
@@ -714,13 +736,19 @@ def config_sweep(ep, dev, stream, flush_l2, n_steps: int) -> list:
         for _ in range(3):
             flush_l2()
             step()
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_steps)]
+        def ev():
+            return torch.cuda.Event(enable_timing=True)
+        evs = [(ev(), None, ev()) for _ in range(n_steps)]
         for e in evs:
             flush_l2()
             step(e)
+        evm = [(ev(), ev(), ev()) for _ in range(n_steps)]
+        for e in evm:
+            flush_l2()
+            step(e)
         torch.cuda.synchronize(dev)
-        t = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[0].elapsed_time(e[2])]
-                      for e in evs]).mean(axis=0) * 1e-3
+        t = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])] for e in evm]).mean(axis=0) * 1e-3
+        t = np.append(t, np.mean([e[0].elapsed_time(e[2]) for e in evs]) * 1e-3)
         ab = algorithmic_bytes(cfg, R)
         disp_b, comb_b = ab["layout"] + ab["dispatch_nvfp4"], ab["combine"]
         res.append({

@@ -1,16 +1,8 @@
-// Split programmatic-dependent-launch controls and bulk asynchronous shared -> global copies,
-// for kernels that do work before waiting on the previous kernel in the stream.
+// Bulk asynchronous shared -> global copies (cp.async.bulk) and the proxy fence they need.
 #pragma once
 #include <cstdint>
 
 namespace ep {
-
-// Wait until every earlier kernel in the stream has completed and its writes are visible.
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-// Let the next kernel in the stream start launching (its own wait still orders its reads).
-__device__ __forceinline__ void pdl_trigger() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
 
 // Shared-memory bytes written by ordinary stores must be ordered before the copy engine reads
 // them: every writer runs fence_proxy_async_smem(), then a barrier, then the copies are issued.

@@ -133,7 +133,7 @@ ep_combine_bwd_kernel(const uint16_t *__restrict__ g, const uint16_t *__restrict
     __shared__ int s_rows[KMAX];
     __shared__ float s_p[KMAX];
     __shared__ float s_red[kCombineThreads / 32][KMAX];
-    pdl_begin();
+    pdl_wait();
     if (load_status(status)) return;
     if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: zero gradient rows
         fill_group_padding(blockIdx.x / fparts, blockIdx.x % fparts, fparts, pad, row_offsets, src_info,

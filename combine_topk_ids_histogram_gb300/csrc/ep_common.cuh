@@ -21,14 +21,29 @@ constexpr unsigned kFullMask = 0xffffffffu;
 __device__ __forceinline__ uint4 ld_stream(const void *p) { return __ldcs(reinterpret_cast<const uint4 *>(p)); }
 __device__ __forceinline__ void st_stream(void *p, uint4 v) { __stcs(reinterpret_cast<uint4 *>(p), v); }
 
-// Programmatic dependent launch.  Every kernel first waits until the kernel before it in the
-// stream has completed and its memory is visible, and only then lets the next kernel start
-// launching; so a kernel never reads anything before all earlier work in the stream is done,
-// while the next kernel's launch and ramp-up overlap this kernel.  Both are no-ops when the
-// kernel was launched without the programmatic-serialization attribute.
+// Programmatic dependent launch.  Every kernel first waits (griddepcontrol.wait) until the
+// kernel before it in the stream has completed and its memory is visible, so it never reads
+// anything before all earlier work in the stream is done.
+//   pdl_begin: grids whose CTAs are all resident at once (persistent grids, the layout) then
+//              let the next kernel start launching, so its launch and ramp-up overlap this
+//              kernel's run.
+//   pdl_wait:  grids with more CTAs than fit at once only wait; the next kernel launches as
+//              their CTAs finish.  Signalled early, the next kernel's CTAs would take SM slots
+//              this grid's later CTAs still need, and sit waiting for it: on GB300 a persistent
+//              combine launched that way behind a 32,768-CTA per-token dispatch made the pair
+//              30% slower (1157 against 886 us).
+// All are no-ops when the kernel was launched without the programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_begin() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// pdl_begin for grids that fit in one wave (no more CTAs than SMs), else pdl_wait.
+__device__ __forceinline__ void pdl_begin_if_one_wave() {
+    unsigned sms;
+    asm("mov.u32 %0, %%nsmid;" : "=r"(sms));
+    if (gridDim.x * gridDim.y * gridDim.z <= sms) pdl_begin();
+    else pdl_wait();
 }
 
 // Status word of the layout: read once per CTA; a non-zero word means "write nothing".

@@ -61,7 +61,7 @@ ep_dispatch_nvfp4_kernel(const uint16_t *__restrict__ x, int T, int H, int K, in
     // early == 1: the kernel directly follows the layout of the same call (which let it launch
     //             only once every earlier kernel had completed), so x is read and quantised
     //             while the layout still runs, and the layout's outputs are read after the wait.
-    if (!early) pdl_begin();
+    if (!early) pdl_wait();
     if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: a group's padding rows
         if (!load_status(status))
             fill_group_padding_call(blockIdx.x / fparts, blockIdx.x % fparts, fparts, pad, row_offsets,
@@ -101,7 +101,7 @@ ep_dispatch_nvfp4_kernel(const uint16_t *__restrict__ x, int T, int H, int K, in
         if (isinf(g)) g = FLT_MAX;
     }
     if (early) {
-        pdl_begin();
+        pdl_wait();
         if (t < T) {
             if (tid < K) my_row = row_of[(size_t)t * K + tid];
             else if (tid == K && S) my_row = row_offsets[E] + t;
@@ -156,7 +156,7 @@ ep_dispatch_bf16_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int
                         const int32_t *__restrict__ row_offsets, const int32_t *__restrict__ src_info,
                         const int32_t *__restrict__ status, uint16_t *__restrict__ out, PadFill f0) {
     __shared__ int s_rows[kMaxRowsPerToken];
-    pdl_begin();
+    pdl_wait();
     if (load_status(status)) return;
     if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: a group's padding rows
         fill_group_padding_call(blockIdx.x / fparts, blockIdx.x % fparts, fparts, pad, row_offsets,
@@ -212,7 +212,7 @@ ep_dispatch_fp8_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int 
                        const int32_t *__restrict__ status, uint8_t *__restrict__ out_fp8,
                        float *__restrict__ out_scales, PadFill f0, PadFill f1) {
     __shared__ int s_rows[kMaxRowsPerToken];
-    pdl_begin();
+    pdl_wait();
     if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: a group's padding rows
         if (!load_status(status))
             fill_group_padding_call(blockIdx.x / fparts, blockIdx.x % fparts, fparts, pad, row_offsets,

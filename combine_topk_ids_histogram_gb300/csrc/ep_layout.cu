@@ -223,7 +223,7 @@ ep_layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int
     __shared__ int s_last;
     __shared__ int s_warp[kLayoutWarps];
 
-    pdl_begin();
+    pdl_begin_if_one_wave();
     const int tid = threadIdx.x, lane = tid & 31;
     const int j = blockIdx.x;
     const int t0 = j * tile_t;
@@ -368,7 +368,7 @@ ep_layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int 
     extern __shared__ int smem[];
     int *s_whist = smem;                       // [kLayoutWarps][E]
     int *s_ids = smem + kLayoutWarps * E;      // [tile_t * K]
-    pdl_begin();
+    pdl_begin_if_one_wave();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int j = blockIdx.x;
     const int t0 = j * tile_t;

@@ -21,7 +21,7 @@ constexpr int kRoutingWarps = kRoutingThreads / 32;
 __global__ void __launch_bounds__(kRoutingThreads)
 ep_map_to_topk_kernel(const uint8_t *__restrict__ map, const float *__restrict__ dense, int T, int E,
                       int K, int32_t *__restrict__ ids, float *__restrict__ probs) {
-    pdl_begin();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const unsigned lt_mask = (1u << lane) - 1u;
     for (int t = blockIdx.x * kRoutingWarps + (threadIdx.x >> 5); t < T; t += gridDim.x * kRoutingWarps) {
@@ -75,7 +75,7 @@ __device__ __forceinline__ unsigned byte_mask16(uint4 v) {
 __global__ void __launch_bounds__(kRoutingThreads)
 ep_map_to_topk_wide_kernel(const uint8_t *__restrict__ map, const float *__restrict__ dense, int T,
                            int E, int K, int32_t *__restrict__ ids, float *__restrict__ probs) {
-    pdl_begin();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int nchunk = E / 16;                    // 16-byte chunks per map row
     for (int t = blockIdx.x * kRoutingWarps + (threadIdx.x >> 5); t < T; t += gridDim.x * kRoutingWarps) {
@@ -131,7 +131,7 @@ ep_map_to_topk_wide_kernel(const uint8_t *__restrict__ map, const float *__restr
 __global__ void __launch_bounds__(kRoutingThreads)
 ep_indices_to_multihot_kernel(const int32_t *__restrict__ ids, const float *__restrict__ probs, int T,
                               int K, int E, uint8_t *__restrict__ map, float *__restrict__ dense) {
-    pdl_begin();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     for (int t = blockIdx.x * kRoutingWarps + (threadIdx.x >> 5); t < T; t += gridDim.x * kRoutingWarps) {
         const int my_id = lane < K ? ids[(size_t)t * K + lane] : -1;
