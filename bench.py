@@ -459,6 +459,7 @@ def run_ours(args, cfg):
         raise RuntimeError("padded or routing-map layout reported an error on the benchmark workload")
     R_pad = int(Lp.row_offsets[Lp.G].item())
     static = static_routing_step(ep, dev, stream, flush_l2, nb)
+    graphs = graph_replay(ep, dev, stream, flush_l2, nb)
     sweep = config_sweep(ep, dev, stream, flush_l2, min(nb, 100)) if not args.no_sweep else None
 
     # ---- e2e through the public API with pinned host buffers ----
@@ -567,6 +568,7 @@ def run_ours(args, cfg):
                          f"{PAD} rows ({R_pad} rows, {R_pad - R} of them padding, written as an "
                          f"all-zero token)"),
         "static_routing_step": static,
+        "graph_replay": graphs,
         "configs_sweep": sweep,
         "e2e": {"value": ws * T * e2e_steps / e2e_t, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
@@ -763,6 +765,72 @@ def config_sweep(ep, dev, stream, flush_l2, n_steps: int) -> list:
             "frac_of_8TB/s": {"step": (disp_b + comb_b) / t[2] / 8e12},
         })
         del x, y, rows, out, L
+        torch.cuda.empty_cache()
+    return res
+
+
+def graph_replay(ep, dev, stream, flush_l2, n_steps: int) -> list:
+    """The benchmark step (fused layout + NVFP4 call, then combine) captured once in a CUDA
+    graph and replayed, against the same step launched call by call, on the tiny workload
+    (launch-bound) and the DSv3 one.  L2 is flushed before each step; events at each step's
+    start and end.  Replays read the buffers captured in the graph."""
+    import torch
+    res = []
+    for name in ("tiny", "dsv3"):
+        cfg = W.CONFIGS[name]
+        C = cfg.rerun_C if cfg.rerun_C else cfg.capacity
+        T, H, E, K, S, P = cfg.T, cfg.H, cfg.E, cfg.K, cfg.S, cfg.P
+        ids_h, probs_h = W.make_routing(cfg)
+        ids = torch.from_numpy(ids_h).to(dev)
+        probs = torch.from_numpy(probs_h).to(dev)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(9500 + cfg.index)
+        x = torch.randn(T, H, device=dev, generator=gen).to(torch.bfloat16)
+        R_max = W.r_max(cfg)
+        y = torch.randn(R_max, H, device=dev, generator=gen).to(torch.bfloat16)
+        L = ep.Layout(T, K, E, P, bool(S), device=dev)
+        rows = (torch.empty(R_max, H // 2, dtype=torch.uint8, device=dev),
+                torch.empty(R_max, H // 16, dtype=torch.uint8, device=dev),
+                torch.empty(R_max, dtype=torch.bfloat16, device=dev),
+                torch.empty(E + S + 1, dtype=torch.int32, device=dev))
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+
+        def step(st):
+            ep.dispatch_layout_nvfp4(ids, x, E, P, C, bool(S), out_layout=L, out=rows, stream=st)
+            ep.combine(y, probs, L, out=out, stream=st)
+
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            step(cap)                      # the first call sets up the launch configuration
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            step(cap)
+        torch.cuda.synchronize(dev)
+
+        def timed(run):
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n_steps)]
+            for _ in range(3):
+                flush_l2()
+                run()
+            for a, b in evs:
+                flush_l2()
+                a.record(stream)
+                run()
+                b.record(stream)
+            torch.cuda.synchronize(dev)
+            return float(np.mean([a.elapsed_time(b) for a, b in evs])) * 1e-3
+
+        eager_s = timed(lambda: step(stream))
+        graph_s = timed(g.replay)
+        if ep.read_status(L) != 0:
+            raise RuntimeError(f"layout status on workload {name}")
+        res.append({"workload": name, "T": T, "hidden": H, "steps": n_steps,
+                    "us_per_step": {"launched": eager_s * 1e6, "graph": graph_s * 1e6},
+                    "tokens/s": {"launched": T / eager_s, "graph": T / graph_s}})
+        del g, x, y, rows, out, L
         torch.cuda.empty_cache()
     return res
 
