@@ -592,11 +592,23 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
     int *hist = s_whist + warp * EP;
     {
         int bad = 0;
-        // the warp's own run, so its histogram needs no second pass over shared memory
+        // the warp's own run, so its histogram needs no second pass over shared memory; all of
+        // a lane's ids (at most kClMaxIds / kClThreads) are requested before the first is used
+        constexpr int kIdsPerLane = kClMaxIds / kClThreads;
+        static_assert(kIdsPerLane * kClThreads == kClMaxIds, "whole ids per lane");
+        int idv[kIdsPerLane];
+#pragma unroll
+        for (int j = 0; j < kIdsPerLane; ++j) {
+            const int i = w0 + lane + 32 * j;
+            idv[j] = i < w1 ? ids[(size_t)t0 * K + i] : -1;
+        }
         int tk = (w0 + lane) / K, kk = (w0 + lane) - tk * K;
         const int step_t = 32 / K, step_k = 32 - step_t * K;
-        for (int i = w0 + lane; i < w1; i += 32) {
-            int id = ids[(size_t)t0 * K + i];
+#pragma unroll
+        for (int j = 0; j < kIdsPerLane; ++j) {
+            const int i = w0 + lane + 32 * j;
+            if (i >= w1) break;
+            int id = idv[j];
             if (bad_id(id, E)) {
                 bad = 1;
                 id = -1;
