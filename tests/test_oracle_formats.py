@@ -153,3 +153,13 @@ def test_encoders_terminate_outside_the_domain():
     # still return instead of searching forever.
     assert oracle.e2m1_encode(float("nan")) in range(16)
     assert oracle.e4m3_encode(float("nan")) in range(256)
+
+
+def test_every_finite_e4m3_value_is_an_f16_value():
+    """The dispatch kernels decode an E4M3 block scale through the hardware E4M3 -> f16 -> fp32
+    conversions, which is exact only if every finite E4M3 value (448 down to the subnormal
+    2^-9) is an f16 value.  f16 has 11 significant bits and normal exponents down to 2^-14, so
+    the subnormals need the f16 subnormals (down to 2^-24)."""
+    vals = np.array([oracle.e4m3_decode(c) for c in range(0x7F)], dtype=np.float64)
+    assert vals[0] == 0.0 and vals.max() == 448.0 and vals[1] == 2.0 ** -9
+    assert np.array_equal(vals.astype(np.float16).astype(np.float64), vals)
