@@ -1,10 +1,21 @@
-"""Parity at the five workloads' full sizes, in the launch configuration the benchmark times.
+"""Parity at the five workloads' full sizes, every element compared, in the launch configuration
+the benchmark times.
 
-The layout is compared in full (the oracle's layout is cheap at any size).  NVFP4 rows and
-combine / backward outputs are compared on sampled tokens (including every outlier and
-all-zero row), each computed by the oracle on a one-token problem built from the full
-workload's inputs.  The large DeepSeek-V3-like microbatch must raise the overflow flag at
-capacity 20000 with every output untouched, then pass in full at capacity 40000."""
+Each output the oracle defines is compared in full against the oracle run on the same seeded
+inputs:
+* the layout (row_offsets, row_of, src_info, expert_ids, part_tokens, status);
+* every NVFP4 row (codes, E4M3 block scales, bf16 inverse scales), from the separate layout +
+  dispatch calls and from the fused layout + NVFP4 call the benchmark step makes, and the rows
+  past R, which keep the oracle's fill value;
+* every BF16 row;
+* every combined token;
+* at the Qwen3-like layer, both backward passes: every grad_y row, every grad_p entry and every
+  token of the dispatch backward pass.
+
+The oracle's binary64 combine sums are taken in token chunks, so host memory stays bounded.
+The large DeepSeek-V3-like microbatch must raise the overflow flag at capacity 20000 with every
+output untouched, then pass in full at capacity 40000.
+"""
 import numpy as np
 import pytest
 import torch
@@ -12,11 +23,14 @@ import torch
 import oracle
 import workloads as W
 from gpu_helpers import (abs_dots, assert_close_bf16, assert_close_gradp, check_layout, dev, dev_bf16,
-                         host_bf16, mini_layout_for_token, new_layout)
+                         host_bf16, new_layout)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
-N_SAMPLE = 48
+FILL8 = 0xA5            # the oracle's fill byte for rows it does not write
+FILL16 = 0xA5A5         # ... and its 16-bit fill
+CHUNK_T = 2048          # tokens per oracle combine chunk (binary64 sums: CHUNK_T * H * 8 bytes)
+CHUNK_R = 16384         # rows per host comparison chunk
 _CACHE = {}
 
 
@@ -35,88 +49,131 @@ def ep():
     return ep
 
 
-def sample_tokens(cfg, x, rng):
-    xf = np.abs(W.f32_from_bf16_bits(x[:, :64]))
-    special = np.flatnonzero((xf.max(1) == 0) | (xf.max(1) > 20))[:16]
-    picks = rng.choice(cfg.T, size=N_SAMPLE, replace=False)
-    return np.unique(np.concatenate([special, picks, [0, cfg.T - 1]]))
+def filled(shape, bits, dtype):
+    """A device buffer holding the oracle's fill pattern (16-bit fills as int16 bit patterns)."""
+    if dtype == torch.uint8:
+        return torch.full(shape, bits, dtype=torch.uint8, device="cuda")
+    return torch.full(shape, bits - 65536 if bits >= 32768 else bits, dtype=torch.int16, device="cuda")
 
 
-def check_nvfp4_rows(fp4, sc, inv, ref, x, toks, S, E):
-    for t in toks:
-        c, s, i = oracle.nvfp4_quantize_row(x[t])
-        rows = [r for r in ref.row_of[t] if r >= 0] + ([ref.row_offsets[E] + t] if S else [])
-        for r in rows:
-            assert np.array_equal(fp4[r].cpu().numpy(), c), (t, r)
-            assert np.array_equal(sc[r].cpu().numpy(), s), (t, r)
-            assert int(host_bf16(inv[r:r + 1])[0]) == i, (t, r)
+def nvfp4_buffers(R_max, H, E, S):
+    return (filled((R_max, H // 2), FILL8, torch.uint8), filled((R_max, H // 16), FILL8, torch.uint8),
+            filled((R_max,), FILL16, torch.int16).view(torch.bfloat16),
+            torch.full((E + S + 1,), -7, dtype=torch.int32, device="cuda"))
 
 
-def check_combine_tokens(out, y_host, probs, ids, ref, toks, E, S, weighted=True):
+def assert_rows_equal(got: torch.Tensor, ref: np.ndarray, what: str):
+    """Bit-exact comparison of a device buffer with the oracle's, CHUNK_R rows at a time."""
+    assert got.shape[0] == ref.shape[0], (what, got.shape, ref.shape)
+    g = got.view(torch.int16) if got.dtype == torch.bfloat16 else got
+    for a in range(0, ref.shape[0], CHUNK_R):
+        b = min(ref.shape[0], a + CHUNK_R)
+        h = g[a:b].cpu().numpy()
+        r = ref[a:b]
+        if h.dtype != r.dtype:
+            h = h.view(r.dtype)
+        if not np.array_equal(h, r):
+            bad = np.argwhere(h != r)[0]
+            raise AssertionError(f"{what}: first difference at row {a + bad[0]}, index {tuple(bad[1:])}: "
+                                 f"gpu {h[tuple(bad)]} oracle {r[tuple(bad)]}")
+
+
+def token_slice(ref, t0, t1):
+    """The oracle layout restricted to tokens [t0, t1): the same rows, the shared row of token t
+    still at row_offsets[E] + t (the oracle computes it from the chunk's first token)."""
+    sub = oracle.Layout(ref)
+    sub["row_of"] = np.ascontiguousarray(ref.row_of[t0:t1])
+    ro = ref.row_offsets.copy()
+    ro[ref.E] += t0
+    sub["row_offsets"] = ro
+    sub["T"] = t1 - t0
+    return sub
+
+
+def check_combine_full(out, y_host, probs, ref, what, weighted=True):
+    """Every token of combine (probs given) or of the dispatch backward pass (weighted False)
+    against the oracle's binary64 sums."""
     got = host_bf16(out)
-    for t in toks:
-        L1, src = mini_layout_for_token(ref, t, ids[t], E, S)
-        y1 = np.zeros((L1.R_max, y_host.shape[1]), np.uint16)
-        ok = src >= 0
-        y1[ok] = y_host[src[ok]]
-        p1 = probs[t:t + 1] if weighted else None
-        _, r64 = oracle.combine(y1, p1, L1, want64=True)
-        assert_close_bf16(got[t:t + 1], r64, f"token {t}")
+    for t0 in range(0, ref.T, CHUNK_T):
+        t1 = min(ref.T, t0 + CHUNK_T)
+        sub = token_slice(ref, t0, t1)
+        p = probs[t0:t1] if weighted else None
+        _, r64 = oracle.combine(y_host, p, sub, want64=True)
+        assert_close_bf16(got[t0:t1], r64, f"{what}, tokens {t0}..{t1}")
 
 
-def run_full(ep, cfg, C=None, backward=False):
+def check_nvfp4_full(bufs, ref_rows, what):
+    fp4, sc, inv, so = bufs
+    rfp4, rsc, rinv, rso = ref_rows
+    assert np.array_equal(so.cpu().numpy(), rso), what
+    assert_rows_equal(fp4, rfp4, f"{what}: E2M1 codes")
+    assert_rows_equal(sc, rsc, f"{what}: E4M3 block scales")
+    assert_rows_equal(inv, rinv, f"{what}: inverse scales")
+
+
+def run_full(ep, cfg, C=None, backward=False, bf16=False):
     C = cfg.capacity if C is None else C
     T, H, E, K, S, P = cfg.T, cfg.H, cfg.E, cfg.K, cfg.S, cfg.P
     inp, y_host = inputs(cfg)
     x, ids, probs = inp["x"], inp["topk_ids"], inp["probs"]
     ref = oracle.layout(ids, E, P=P, C=C, S=S)
-    L = new_layout(ep, T, K, E, P, S)
-    ep.dispatch_layout(dev(ids), E, P, C, bool(S), out=L)
-    check_layout(L, ref, ep)
     R_max = ref.R_max
-    fp4 = torch.full((R_max, H // 2), 0xA5, dtype=torch.uint8, device="cuda")
-    sc = torch.full((R_max, H // 16), 0xA5, dtype=torch.uint8, device="cuda")
-    inv = torch.full((R_max,), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
-    so = torch.full((E + S + 1,), -7, dtype=torch.int32, device="cuda")
-    ep.dispatch_nvfp4(dev_bf16(x), L, out=(fp4, sc, inv, so))
+    xd, idd, pd = dev_bf16(x), dev(ids), dev(probs)
+
+    # separate calls: layout, NVFP4 dispatch, combine
+    L = new_layout(ep, T, K, E, P, S)
+    ep.dispatch_layout(idd, E, P, C, bool(S), out=L)
+    check_layout(L, ref, ep)
+    bufs = nvfp4_buffers(R_max, H, E, S)
+    ep.dispatch_nvfp4(xd, L, out=bufs)
     yd = dev_bf16(y_host)
-    out = torch.full((T, H), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
-    ep.combine(yd, dev(probs), L, out=out)
+    out = filled((T, H), FILL16, torch.int16).view(torch.bfloat16)
+    ep.combine(yd, pd, L, out=out)
+    # the fused layout + NVFP4 call
+    Lf = new_layout(ep, T, K, E, P, S)
+    fbufs = nvfp4_buffers(R_max, H, E, S)
+    ep.dispatch_layout_nvfp4(idd, xd, E, P, C, bool(S), out_layout=Lf, out=fbufs)
     torch.cuda.synchronize()
+    check_layout(Lf, ref, ep)
+
+    ref_rows = oracle.dispatch_nvfp4(x, ref, fill=FILL8)   # every row untouched on overflow
+    check_nvfp4_full(bufs, ref_rows, f"{cfg.name} NVFP4 dispatch")
+    check_nvfp4_full(fbufs, ref_rows, f"{cfg.name} fused layout + NVFP4")
+    del ref_rows, fbufs
     if ref.status:
-        assert (fp4 == 0xA5).all() and (sc == 0xA5).all() and (so == -7).all()
-        assert (inv.view(torch.int16) == -1).all() and (out.view(torch.int16) == -1).all()
+        assert (out.view(torch.int16) == FILL16 - 65536).all(), "combine wrote on overflow"
         return ref
-    rng = np.random.default_rng(cfg.index)
-    toks = sample_tokens(cfg, x, rng)
-    assert np.array_equal(so.cpu().numpy(), ref.row_offsets)
-    check_nvfp4_rows(fp4, sc, inv, ref, x, toks, S, E)
-    # rows past R are untouched
-    assert (fp4[ref.R:] == 0xA5).all() and (inv.view(torch.int16)[ref.R:] == -1).all()
-    check_combine_tokens(out, y_host, probs, ids, ref, toks, E, S)
+    check_combine_full(out, y_host, probs, ref, f"{cfg.name} combine")
+    if bf16:
+        rows = filled((R_max, H), FILL16, torch.int16).view(torch.bfloat16)
+        ep.dispatch_bf16(xd, L, out=rows)
+        assert_rows_equal(rows, oracle.dispatch_bf16(x, ref, fill=FILL16), f"{cfg.name} BF16 dispatch")
+        del rows
     if backward:
         g = W.make_grad_out(cfg)
-        gy, gp = ep.combine_bwd(dev_bf16(g), yd, dev(probs), L)
+        gy = filled((R_max, H), FILL16, torch.int16).view(torch.bfloat16)
+        gp = torch.full((T, K), float("nan"), dtype=torch.float32, device="cuda")
+        ep.combine_bwd(dev_bf16(g), yd, pd, L, out=(gy, gp))
+        rgy, rgp, rgy64 = oracle.combine_bwd(g, y_host, probs, ref, want64=True, fill=FILL16)
+        R = ref.R
         gyh = host_bf16(gy)
-        for t in toks:
-            L1, src = mini_layout_for_token(ref, t, ids[t], E, S)
-            y1 = np.zeros((L1.R_max, H), np.uint16)
-            y1[src >= 0] = y_host[src[src >= 0]]
-            _, rgp, rgy64 = oracle.combine_bwd(g[t:t + 1], y1, probs[t:t + 1], L1, want64=True)
-            for r1 in range(L1.R):
-                assert_close_bf16(gyh[src[r1]][None], rgy64[r1][None], f"grad_y token {t}")
-            assert_close_gradp(gp[t:t + 1].cpu().numpy(), rgp, abs_dots(g[t:t + 1], y1, L1.row_of),
-                               f"grad_p token {t}")
+        for a in range(0, R, CHUNK_R):
+            b = min(R, a + CHUNK_R)
+            assert_close_bf16(gyh[a:b], rgy64[a:b], f"{cfg.name} grad_y rows {a}..{b}")
+        assert np.array_equal(gyh[R:], rgy[R:]), "grad_y rows past R were written"
+        assert_close_gradp(gp.cpu().numpy(), rgp, abs_dots(g, y_host, ref.row_of), f"{cfg.name} grad_p")
+        del gyh, rgy, rgy64
         gr = W.make_grad_rows(cfg)
-        gx = ep.dispatch_bwd(dev_bf16(gr), L)
-        check_combine_tokens(gx, gr, probs, ids, ref, toks, E, S, weighted=False)
+        gx = filled((T, H), FILL16, torch.int16).view(torch.bfloat16)
+        ep.dispatch_bwd(dev_bf16(gr), L, out=gx)
+        check_combine_full(gx, gr, probs, ref, f"{cfg.name} dispatch backward", weighted=False)
     return ref
 
 
 @pytest.mark.parametrize("name", ["tiny", "qwen3", "dsv3", "mixtral"])
 def test_full_size(ep, name):
     cfg = W.CONFIGS[name]
-    ref = run_full(ep, cfg, backward=(name == "qwen3"))
+    ref = run_full(ep, cfg, backward=(name == "qwen3"), bf16=(name in ("tiny", "mixtral", "dsv3")))
     assert ref.status == 0
 
 
@@ -128,25 +185,6 @@ def test_full_size_overflow_then_rerun(ep):
     assert ref.status == 0
 
 
-def test_full_size_fused_call(ep):
-    """ep_dispatch_layout_nvfp4 on the DSv3-like layer, as the benchmark step calls it."""
-    cfg = W.CONFIGS["dsv3"]
-    T, H, E, K, S, P, C = cfg.T, cfg.H, cfg.E, cfg.K, cfg.S, cfg.P, cfg.capacity
-    inp, _ = inputs(cfg)
-    x, ids = inp["x"], inp["topk_ids"]
-    ref = oracle.layout(ids, E, P=P, C=C, S=S)
-    L = new_layout(ep, T, K, E, P, S)
-    out = (torch.full((ref.R_max, H // 2), 0xA5, dtype=torch.uint8, device="cuda"),
-           torch.full((ref.R_max, H // 16), 0xA5, dtype=torch.uint8, device="cuda"),
-           torch.full((ref.R_max,), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16),
-           torch.full((E + S + 1,), -7, dtype=torch.int32, device="cuda"))
-    ep.dispatch_layout_nvfp4(dev(ids), dev_bf16(x), E, P, C, bool(S), out_layout=L, out=out)
-    check_layout(L, ref, ep)
-    toks = sample_tokens(cfg, x, np.random.default_rng(31))
-    check_nvfp4_rows(*out[:3], ref, x, toks, S, E)
-    assert np.array_equal(out[3].cpu().numpy(), ref.row_offsets)
-
-
 def test_full_size_fp8(ep):
     cfg = W.CONFIGS["dsv3"]
     T, H, E, K, S, P, C = cfg.T, cfg.H, cfg.E, cfg.K, cfg.S, cfg.P, cfg.capacity
@@ -155,17 +193,17 @@ def test_full_size_fp8(ep):
     ref = oracle.layout(ids, E, P=P, C=C, S=S)
     L = new_layout(ep, T, K, E, P, S)
     ep.dispatch_layout(dev(ids), E, P, C, bool(S), out=L)
-    codes, scales = ep.dispatch_fp8(dev_bf16(x), L)
-    for t in sample_tokens(cfg, x, np.random.default_rng(32)):
-        c, s = oracle.fp8_quantize_row(x[t])
-        for r in [r for r in ref.row_of[t] if r >= 0] + [ref.row_offsets[E] + t]:
-            assert np.array_equal(codes[r].cpu().numpy(), c), (t, r)
-            assert np.array_equal(scales[r].cpu().numpy().view(np.uint32), s.view(np.uint32)), (t, r)
+    codes = filled((ref.R_max, H), FILL8, torch.uint8)
+    scales = filled((ref.R_max, 4 * (H // 128)), FILL8, torch.uint8)
+    ep.dispatch_fp8(dev_bf16(x), L, out=(codes, scales.view(torch.float32)))
+    rc, rs = oracle.dispatch_fp8(x, ref, fill=FILL8)
+    assert_rows_equal(codes, rc, "FP8 codes")
+    assert_rows_equal(scales, rs.view(np.uint8).reshape(ref.R_max, -1), "FP8 block scales")
 
 
 @pytest.mark.parametrize("name,pad,cap", [("dsv3", 128, None), ("dsv3_static", 128, 36864)])
 def test_full_size_padded(ep, name, pad, cap):
-    """Padded layout in full, NVFP4 rows and combine on sampled tokens, every padding row."""
+    """Padded layout, every NVFP4 row (padding rows included) and every combined token."""
     cfg = W.CONFIGS[name]
     T, H, E, K, S, P, C = cfg.T, cfg.H, cfg.E, cfg.K, cfg.S, cfg.P, cfg.capacity
     inp = W.make_inputs(cfg)
@@ -180,29 +218,12 @@ def test_full_size_padded(ep, name, pad, cap):
     assert np.array_equal(L.row_of.cpu().numpy(), ref.row_of)
     assert np.array_equal(L.expert_ids.cpu().numpy()[:ref.R], ref.expert_ids[:ref.R])
     assert np.array_equal(L.src_info.cpu().numpy()[:ref.R], ref.src_info[:ref.R])
-    fp4, sc, inv, so = ep.dispatch_nvfp4(dev_bf16(x), L)
-    toks = sample_tokens(cfg, x, np.random.default_rng(33))
-    check_nvfp4_rows(fp4, sc, inv, ref, x, toks, S, E)
-    pad_rows = torch.from_numpy(np.flatnonzero(ref.src_info[:ref.R, 0] < 0)).cuda()
-    if pad_rows.numel():
-        assert (fp4[pad_rows] == 0).all() and (sc[pad_rows] == 0).all()
-        assert (inv.view(torch.int16)[pad_rows] == 0x3F80).all()
+    bufs = nvfp4_buffers(ref.R_max, H, E, S)
+    ep.dispatch_nvfp4(dev_bf16(x), L, out=bufs)
+    check_nvfp4_full(bufs, oracle.dispatch_nvfp4(x, ref, fill=FILL8), f"{name} padded NVFP4")
     y_host = np.resize(W.make_expert_out(cfg), (ref.R_max, H)).astype(np.uint16)
     out = ep.combine(dev_bf16(y_host), dev(probs), L)
-    # each sampled token through a one-token oracle problem, rows mapped into the padded layout
-    got = host_bf16(out)
-    for t in toks:
-        L1 = oracle.layout(ids[t][None, :], E, S=S)
-        src = np.full(L1.R_max, -1, np.int64)
-        for k in range(K):
-            if L1.row_of[0, k] >= 0:
-                src[L1.row_of[0, k]] = ref.row_of[t, k]
-        if S:
-            src[L1.row_offsets[E]] = ref.row_offsets[E] + t
-        y1 = np.zeros((L1.R_max, H), np.uint16)
-        y1[src >= 0] = y_host[src[src >= 0]]
-        _, r64 = oracle.combine(y1, probs[t:t + 1], L1, want64=True)
-        assert_close_bf16(got[t:t + 1], r64, f"token {t}")
+    check_combine_full(out, y_host, probs, ref, f"{name} padded combine")
 
 
 def test_full_size_routing_map_layout(ep):
