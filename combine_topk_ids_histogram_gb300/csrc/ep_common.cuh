@@ -38,11 +38,11 @@ __device__ __forceinline__ void pdl_begin() {
     pdl_wait();
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
-// pdl_begin for grids that fit in one wave (no more CTAs than SMs), else pdl_wait.
-__device__ __forceinline__ void pdl_begin_if_one_wave() {
-    unsigned sms;
-    asm("mov.u32 %0, %%nsmid;" : "=r"(sms));
-    if (gridDim.x * gridDim.y * gridDim.z <= sms) pdl_begin();
+// pdl_begin for grids that fit in one wave, else pdl_wait.  `one_wave` comes from the host,
+// which compares the grid with the device's SM count (the %nsmid register only bounds the SM
+// ids and may exceed the count).
+__device__ __forceinline__ void pdl_begin_if(int one_wave) {
+    if (one_wave) pdl_begin();
     else pdl_wait();
 }
 

@@ -91,6 +91,28 @@ inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sm
     return launch_result(cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...));
 }
 
+// SM count of the current device (0 on error), looked up once per device.
+inline int device_sm_count() {
+    constexpr int kMaxDev = 64;
+    static int cached[kMaxDev];   // 0: not looked up
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < kMaxDev && cached[dev]) return cached[dev];
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < kMaxDev) cached[dev] = sms;
+    return sms;
+}
+
+// Whether a grid of `ctas` blocks is no larger than the SM count, so that all of its blocks are
+// resident at once (one per SM is enough).
+inline int one_wave(int ctas) {
+    const int sms = device_sm_count();
+    return sms > 0 && ctas <= sms ? 1 : 0;
+}
+
 // Blocks of `kernel` that fit on the device at once (SM count x resident blocks per SM),
 // for grids that loop over their work.  Cached per (device, kernel, block size, shared memory).
 template <typename K>

@@ -213,7 +213,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int &t
 __global__ void __launch_bounds__(kLayoutThreads)
 ep_layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int P, int C, int S,
                        int pad, int row_limit, int tile_t, int nTiles, unsigned long long per_magic,
-                       Workspace ws, int32_t *__restrict__ row_offsets,
+                       int one_wave, Workspace ws, int32_t *__restrict__ row_offsets,
                        int32_t *__restrict__ part_tokens, int32_t *__restrict__ status) {
     extern __shared__ int smem[];
     int *s_hist = smem;          // [E]
@@ -223,7 +223,7 @@ ep_layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int
     __shared__ int s_last;
     __shared__ int s_warp[kLayoutWarps];
 
-    pdl_begin_if_one_wave();
+    pdl_begin_if(one_wave);
     const int tid = threadIdx.x, lane = tid & 31;
     const int j = blockIdx.x;
     const int t0 = j * tile_t;
@@ -362,13 +362,14 @@ ep_layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int
 
 __global__ void __launch_bounds__(kLayoutThreads)
 ep_layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int S, int pad,
-                      int row_limit, int tile_t, int nTiles, int nbits, const int32_t *__restrict__ cnt,
+                      int row_limit, int tile_t, int nTiles, int nbits, int one_wave,
+                      const int32_t *__restrict__ cnt,
                       const int32_t *__restrict__ row_offsets, int32_t *__restrict__ row_of,
                       int32_t *__restrict__ src_info, int32_t *__restrict__ expert_ids) {
     extern __shared__ int smem[];
     int *s_whist = smem;                       // [kLayoutWarps][E]
     int *s_ids = smem + kLayoutWarps * E;      // [tile_t * K]
-    pdl_begin_if_one_wave();
+    pdl_begin_if(one_wave);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int j = blockIdx.x;
     const int t0 = j * tile_t;
@@ -875,6 +876,36 @@ inline int launch_cluster_layout(const int32_t *ids, int T, int K, int E, int P,
 
 using namespace ep;
 
+namespace ep {
+namespace {
+
+// The two-kernel layout (count + scan, then rank) with its scratch at `scratch`, which holds at
+// least workspace_bytes(nTiles, E) bytes whose ticket word is zero.
+int launch_tiled_layout(const int32_t *topk_ids, int T, int K, int E, int P, int capacity, int S,
+                        int pad, int row_limit, void *scratch, ep_layout_t *L, cudaStream_t st) {
+    const int tt = tile_tokens(T, K);
+    const int nTiles = num_tiles(T, tt);
+    const int wave = one_wave(nTiles);
+    Workspace ws = carve(scratch, nTiles, E);
+    const size_t smem_count = count_smem_bytes(E, P, tt, K);
+    int rc = launch_pdl(ep_layout_count_kernel, dim3(nTiles), dim3(kLayoutThreads), smem_count, st,
+                        topk_ids, T, K, E, P, capacity, S, pad, row_limit, tt, nTiles,
+                        magic_of(E / P), wave, ws, L->row_offsets, L->part_tokens, L->status);
+    if (rc != EP_OK) return rc;
+    size_t smem_rank = sizeof(int) * ((size_t)kLayoutWarps * E + (size_t)tt * K);
+    if (smem_rank > 48 * 1024 &&
+        cudaFuncSetAttribute(ep_layout_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_rank) != cudaSuccess)
+        return EP_ERR_CUDA;
+    return launch_pdl(ep_layout_rank_kernel, dim3(nTiles), dim3(kLayoutThreads), smem_rank, st,
+                      topk_ids, T, K, E, S, pad, row_limit, tt, nTiles, key_bits(E + 1), wave,
+                      (const int32_t *)ws.cnt, (const int32_t *)L->row_offsets, L->row_of,
+                      L->src_info, L->expert_ids);
+}
+
+}  // namespace
+}  // namespace ep
+
 extern "C" size_t ep_layout_workspace_bytes(int T, int K, int n_experts, int fused_shared) {
     if (!sizes_ok(T, K, n_experts, fused_shared)) return 0;
     int tt = tile_tokens(T, K);
@@ -920,21 +951,7 @@ int launch_layout(const int32_t *topk_ids, int T, int K, int E, int P, int capac
         if (cluster_ctas_used) *cluster_ctas_used = used;
         return rc_cl;
     }
-    Workspace ws = carve(L->workspace, nTiles, E);
-    const size_t smem_count = count_smem_bytes(E, P, tt, K);
-    int rc = launch_pdl(ep_layout_count_kernel, dim3(nTiles), dim3(kLayoutThreads), smem_count, st,
-                        topk_ids, T, K, E, P, capacity, S, pad, row_limit, tt, nTiles,
-                        magic_of(E / P), ws, L->row_offsets, L->part_tokens, L->status);
-    if (rc != EP_OK) return rc;
-    size_t smem_rank = sizeof(int) * ((size_t)kLayoutWarps * E + (size_t)tt * K);
-    if (smem_rank > 48 * 1024 &&
-        cudaFuncSetAttribute(ep_layout_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem_rank) != cudaSuccess)
-        return EP_ERR_CUDA;
-    return launch_pdl(ep_layout_rank_kernel, dim3(nTiles), dim3(kLayoutThreads), smem_rank, st,
-                      topk_ids, T, K, E, S, pad, row_limit, tt, nTiles, key_bits(E + 1),
-                      (const int32_t *)ws.cnt, (const int32_t *)L->row_offsets, L->row_of,
-                      L->src_info, L->expert_ids);
+    return launch_tiled_layout(topk_ids, T, K, E, P, capacity, S, pad, row_limit, L->workspace, L, st);
 }
 
 }  // namespace ep
@@ -1008,12 +1025,13 @@ extern "C" const char *ep_strerror(int code) {
 // For callers that must not allocate device memory at all: code running under a framework
 // whose caching allocator owns the whole device, latency-critical paths where an allocation
 // (and the device synchronisation cudaMalloc/cudaFree can imply) is not acceptable, or
-// runtimes that hand a library only its inputs and outputs.  The scratch lives in a
-// file-scope __device__ array of kNoAllocWorkspaceBytes that every GPU which loads this
-// library keeps until the process exits.  Host code cannot use the array's name as a device
-// address (on the host it is only a stand-in symbol), so the device address is looked up once
-// per device with cudaGetSymbolAddress, with that device current, during the first call on
-// that device.  That first call also zeroes the ticket word; every later call leaves it at zero
+// runtimes that hand a library only its inputs and outputs.  Sizes that fit one thread-block
+// cluster run the single-cluster kernel, which needs no scratch.  Larger sizes run the two-kernel
+// layout with its scratch in a file-scope __device__ array of kNoAllocWorkspaceBytes that every
+// GPU which loads this library keeps until the process exits.  Host code cannot use the array's
+// name as a device address (on the host it is only a stand-in symbol), so the device address is
+// looked up once per device with cudaGetSymbolAddress, with that device current, during the
+// first call on that device.  That first call also zeroes the ticket word; every later call leaves it at zero
 // when it finishes.  All calls share the one array, so calls whose work overlaps on the GPU
 // (other streams, other threads) race on it.
 // ---------------------------------------------------------------------------------------
@@ -1079,20 +1097,10 @@ extern "C" int ep_dispatch_layout_noalloc(const int32_t *topk_ids, int T, int K,
     const int row_limit = layout_rows(L);
 
     cudaStream_t st = as_stream(stream);
-    Workspace ws = carve(scratch, nTiles, E);
-    const size_t smem_count = count_smem_bytes(E, P, tt, K);
-    ep_layout_count_kernel<<<nTiles, kLayoutThreads, smem_count, st>>>(
-        topk_ids, T, K, E, P, capacity, S, 1, row_limit, tt, nTiles, magic_of(E / P), ws, L->row_offsets,
-        L->part_tokens, L->status);
-    rc = launch_result();
-    if (rc != EP_OK) return rc;
-    size_t smem_rank = sizeof(int) * ((size_t)kLayoutWarps * E + (size_t)tt * K);
-    if (smem_rank > 48 * 1024 &&
-        cudaFuncSetAttribute(ep_layout_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem_rank) != cudaSuccess)
-        return EP_ERR_CUDA;
-    ep_layout_rank_kernel<<<nTiles, kLayoutThreads, smem_rank, st>>>(
-        topk_ids, T, K, E, S, 1, row_limit, tt, nTiles, key_bits(E + 1), ws.cnt, L->row_offsets, L->row_of,
-        L->src_info, L->expert_ids);
-    return launch_result();
+    // Sizes that fit one thread-block cluster need no scratch at all: the single-cluster kernel
+    // exchanges its counts through distributed shared memory.
+    int used = 0;
+    rc = launch_cluster_layout(topk_ids, T, K, E, P, capacity, S, 1, row_limit, L, st, &used);
+    if (rc != -1) return rc;
+    return launch_tiled_layout(topk_ids, T, K, E, P, capacity, S, 1, row_limit, scratch, L, st);
 }

@@ -330,19 +330,21 @@ int ep_read_status(const ep_layout_t *L, void *stream, int32_t *host_status);
  * all device memory, latency-critical paths that must not pay for (or synchronise on) an
  * allocation, and runtimes that give a library its inputs and outputs and nothing else.  This
  * entry point computes exactly what ep_dispatch_layout computes, from the same arguments, but
- * takes its scratch from a fixed array inside the library instead of L->workspace
- * (L->workspace and L->workspace_bytes are ignored and may be NULL / 0).  The caller still
- * passes every input and output buffer.
+ * never touches L->workspace (L->workspace and L->workspace_bytes are ignored and may be
+ * NULL / 0).  Sizes whose ids fit one thread-block cluster (the single-cluster layout kernel
+ * ep_dispatch_layout also uses) need no scratch at all; larger sizes run the two-kernel layout
+ * with its scratch in a fixed array inside the library.  The caller still passes every input
+ * and output buffer.
  *
  *   Limit: the sizes must satisfy ep_layout_workspace_bytes(T, K, E, S) <=
- *   EP_NOALLOC_WORKSPACE_BYTES (1 MiB; T = 32768, K = 8, E = 256 needs 131 KiB, and at
- *   K = 8, E = 256 every T up to 522240 fits); larger sizes return EP_ERR_TOO_LARGE and
- *   enqueue nothing.  Every GPU that loads the
- *   library holds that 1 MiB until the process exits.
+ *   EP_NOALLOC_WORKSPACE_BYTES (1 MiB; T = 32768, K = 8, E = 256 needs 128.5 KiB (131,584
+ *   bytes), and at K = 8, E = 256 every T up to 522240 fits); larger sizes return
+ *   EP_ERR_TOO_LARGE and enqueue nothing.  Every GPU that loads the library holds that 1 MiB
+ *   until the process exits.
  *   Set-up: the first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current) and zeroes its first 256 bytes with a
  *   synchronous cudaMemset; make that first call before any stream capture.  Later calls only
- *   enqueue the two layout kernels.
+ *   enqueue the layout kernels.
  *   Sharing: every call on a device uses the same array, and each call leaves it ready for the
  *   next.  Calls whose work overlaps on the GPU (two streams, or two host threads) race on the
  *   array and give undefined results; serialise them.
