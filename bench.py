@@ -21,7 +21,6 @@ import datetime as _dt
 import hashlib
 import json
 import os
-import re
 import subprocess
 import sys
 import time
@@ -89,26 +88,30 @@ def load_peaks() -> tuple[float, str]:
         return 6800.0, "fallback"
 
 
-def kernel_source_hash() -> str:
+COMBINE_SOURCES = ("ep_common.cuh", "ep_padding.cuh", "ep_combine.cu")   # device code of combine's unit
+
+
+def kernel_source_hash(files=COMBINE_SOURCES) -> str:
     h = hashlib.sha256()
-    for f in ("ep_common.cuh", "ep_padding.cuh", "ep_combine.cu"):   # device code of combine's unit
+    for f in files:
         with open(os.path.join(ROOT, "combine_topk_ids_histogram_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str) -> float | None:
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken on
-    the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", f"{kernel}_dsv3.md")
-    if not os.path.exists(path):
+def recorded_traffic(name: str) -> float | None:
+    """DRAM bytes (read + written) per launch from the ncu capture recorded in
+    profiles/<name>.json, if that capture was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{name}.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    text = open(path).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    s = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
-    if not m or not s or s.group(1) != kernel_source_hash():
+    files = tuple(rec.get("source_files", COMBINE_SOURCES))
+    if rec.get("source_sha256_16") != kernel_source_hash(files):
         return None
-    return float(m.group(1))
+    return float(rec["traffic_bytes_per_launch"])
 
 
 # ------------------------------------------------------------------------------------------
@@ -236,6 +239,50 @@ def time_oracle(cfg: W.Config, inp: dict, y: np.ndarray, budget_s: float, T_s: i
         if t_tot >= budget_s or reps >= 8:
             break
     return T_s * reps / t_tot, T_s, reps, t_tot
+
+
+def oracle_ops(cfg: W.Config, elems: int = 1 << 21, reps: int = 3) -> dict:
+    """The oracle as it stands, timed per op on a bounded sample of one workload: T_s tokens
+    drawn by the workload's own recipe (its routing distribution, outliers and zero rows), about
+    `elems` hidden elements in all.  Each op's wall time is the best of `reps`, on one thread.
+    The ops are those the sweep times on the GPU (layout, NVFP4 dispatch, combine), plus the BF16
+    dispatch where the workload names it and, on the Qwen3-like layer, both backward passes.
+    The layout, which touches no hidden elements, runs on the workload's full routing."""
+    import oracle
+    oracle.build()
+    T_s = min(cfg.T, max(64, elems // cfg.H))
+    C = cfg.rerun_C if cfg.rerun_C else cfg.capacity
+    sc = W.scaled(cfg, T=T_s, C=C, rerun_C=None, num_permuted_tokens=None)
+    inp = W.make_inputs(sc)
+    y = W.make_expert_out(sc)
+    x, ids, probs = inp["x"], inp["topk_ids"], inp["probs"]
+    L = oracle.layout(ids, sc.E, P=sc.P, C=sc.capacity, S=sc.S)
+    ids_full = W.make_routing(cfg)[0]
+    ops = {
+        "layout": lambda: oracle.layout(ids_full, cfg.E, P=cfg.P, C=C, S=cfg.S),
+        "dispatch_nvfp4": lambda: oracle.dispatch_nvfp4(x, L),
+        "combine": lambda: oracle.combine(y, probs, L),
+    }
+    if cfg.name in ("tiny", "mixtral"):
+        ops["dispatch_bf16"] = lambda: oracle.dispatch_bf16(x, L)
+    if cfg.name == "qwen3":
+        g = W.make_grad_out(sc)
+        gr = W.make_grad_rows(sc)
+        ops["combine_bwd"] = lambda: oracle.combine_bwd(g, y, probs, L)
+        ops["dispatch_bwd"] = lambda: oracle.dispatch_bwd(gr, L)
+    secs = {}
+    for name, fn in ops.items():
+        best = float("inf")
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            fn()
+            best = min(best, time.perf_counter() - t0)
+        secs[name] = best
+    tokens = {k: (cfg.T if k == "layout" else T_s) for k in secs}
+    return {"kind": "oracle", "cores": 1, "tokens_sampled": T_s, "reps": reps,
+            "sample": f"layout over all {cfg.T} tokens; the other ops on {T_s} tokens drawn by the "
+                      f"workload's recipe (capacity {C}); best of {reps} per op, single-threaded C oracle",
+            "s": secs, "tokens/s": {k: tokens[k] / v for k, v in secs.items()}}
 
 
 def run_reference(args, cfg):
@@ -524,7 +571,7 @@ def run_ours(args, cfg):
     ab[f"dispatch_nvfp4 (pad {PAD})"] = pb["dispatch_nvfp4"]
     peak, peak_kind = load_peaks()
     achieved = ab["combine"] / comb_s / 1e9
-    traffic = recorded_traffic("combine")
+    traffic = recorded_traffic("combine_dsv3")
     kernels = {}
     times = dict(zip(("layout", "dispatch_nvfp4", "combine"), brk))
     times.update(extra)
@@ -547,6 +594,11 @@ def run_ours(args, cfg):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_max / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "dtypes": {"arithmetic": "f32 (quantisation scales, E2M1/E4M3 encoding, combine accumulation)",
+                   "activations": "bf16 (x, expert outputs, combined output)",
+                   "dispatch_out": "nvfp4: e2m1 codes + e4m3 block scales (16 elements) + bf16 inverse "
+                                   "global scale per row",
+                   "probs": "f32"},
         "data": "synthetic (seeded: workloads.CONFIGS['dsv3'])",
         "config": workload_config(cfg),
         "roofline": {"kernel": "ep_combine_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
@@ -584,6 +636,9 @@ def run_ours(args, cfg):
         "clocks": clocks,
         "rows": R,
     }
+    if ws == 1 and not args.no_cpu_baseline and sweep:
+        for entry in sweep:   # the oracle per op on every workload of the sweep
+            entry["cpu_oracle"] = oracle_ops(W.CONFIGS[entry["workload"]])
     if ws == 1 and not args.no_cpu_baseline:
         v, T_s, reps, secs = time_oracle(cfg, inp, y_host, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
@@ -890,6 +945,107 @@ def static_routing_step(ep, dev, stream, flush_l2, n_steps: int) -> dict:
             "calls": "ep_dispatch_layout_routed + ep_dispatch_nvfp4 (+ padding fill) + ep_combine"}
 
 
+ONLY_OPS = ("layout", "layout_noalloc", "dispatch_layout_nvfp4", "dispatch_nvfp4", "dispatch_bf16",
+            "dispatch_fp8", "combine", "combine_bwd", "dispatch_bwd", "indices_to_multihot",
+            "routing_map_layout")
+
+
+def run_only(args, cfg):
+    """One library call alone on one workload, for profiling: only that call's buffers are
+    allocated; the routing comes from the workload's recipe and x / expert outputs / gradients
+    are seeded device draws.  W + K launches, the L2 flushed before each, CUDA events around the
+    K timed ones; prints one JSON line with the mean time and the algorithmic bytes."""
+    import torch
+    import combine_topk_ids_histogram_gb300 as ep
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    T, H, E, K, S, P, C = cfg.T, cfg.H, cfg.E, cfg.K, cfg.S, cfg.P, cfg.capacity
+    R_max = W.r_max(cfg)
+    ids_h, probs_h = W.make_routing(cfg)
+    ids = torch.from_numpy(ids_h).to(dev)
+    probs = torch.from_numpy(probs_h).to(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(9700 + cfg.index)
+
+    def randn(*shape):
+        return torch.randn(*shape, device=dev, generator=gen).to(torch.bfloat16)
+
+    L = ep.Layout(T, K, E, P, bool(S), device=dev)
+    ep.dispatch_layout(ids, E, P, C, bool(S), out=L, stream=stream)
+    op = args.only
+    if op == "layout":
+        fn = lambda: ep.dispatch_layout(ids, E, P, C, bool(S), out=L, stream=stream)
+    elif op == "layout_noalloc":
+        fn = lambda: ep.dispatch_layout_noalloc(ids, E, P, C, bool(S), out=L, stream=stream)
+    elif op in ("dispatch_layout_nvfp4", "dispatch_nvfp4"):
+        x = randn(T, H)
+        rows = (torch.empty(R_max, H // 2, dtype=torch.uint8, device=dev),
+                torch.empty(R_max, H // 16, dtype=torch.uint8, device=dev),
+                torch.empty(R_max, dtype=torch.bfloat16, device=dev),
+                torch.empty(E + S + 1, dtype=torch.int32, device=dev))
+        if op == "dispatch_nvfp4":
+            fn = lambda: ep.dispatch_nvfp4(x, L, out=rows, stream=stream)
+        else:
+            fn = lambda: ep.dispatch_layout_nvfp4(ids, x, E, P, C, bool(S), out_layout=L, out=rows,
+                                                  stream=stream)
+    elif op == "dispatch_bf16":
+        x, out = randn(T, H), torch.empty(R_max, H, dtype=torch.bfloat16, device=dev)
+        fn = lambda: ep.dispatch_bf16(x, L, out=out, stream=stream)
+    elif op == "dispatch_fp8":
+        x = randn(T, H)
+        out = (torch.empty(R_max, H, dtype=torch.uint8, device=dev),
+               torch.empty(R_max, H // 128, dtype=torch.float32, device=dev))
+        fn = lambda: ep.dispatch_fp8(x, L, out=out, stream=stream)
+    elif op in ("combine", "dispatch_bwd"):
+        y, out = randn(R_max, H), torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        if op == "combine":
+            fn = lambda: ep.combine(y, probs, L, out=out, stream=stream)
+        else:
+            fn = lambda: ep.dispatch_bwd(y, L, out=out, stream=stream)
+    elif op == "combine_bwd":
+        y, g = randn(R_max, H), randn(T, H)
+        out = (torch.empty(R_max, H, dtype=torch.bfloat16, device=dev),
+               torch.empty(T, K, dtype=torch.float32, device=dev))
+        fn = lambda: ep.combine_bwd(g, y, probs, L, out=out, stream=stream)
+    elif op == "indices_to_multihot":
+        out = (torch.empty(T, E, dtype=torch.uint8, device=dev), torch.empty(T, E, dtype=torch.float32, device=dev))
+        fn = lambda: ep.indices_to_multihot(ids, probs, E, out=out, stream=stream)
+    else:   # routing_map_layout
+        rmap, dprobs = ep.indices_to_multihot(ids, probs, E)
+        Lm = ep.Layout(T, K, E, P, bool(S), device=dev)
+        mo = (torch.empty(T, K, dtype=torch.int32, device=dev), torch.empty(T, K, dtype=torch.float32, device=dev))
+        fn = lambda: ep.dispatch_layout_routed(E, routing_map=rmap, dense_probs=dprobs, K=K, n_parts=P,
+                                               capacity=C, fused_shared=bool(S), out=Lm, map_out=mo,
+                                               stream=stream)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    sink = torch.empty((), dtype=torch.int32, device=dev)
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        torch.amax(flush_rd, dim=0, out=sink)
+        fn()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for a, b in evs:
+        flush.fill_(1)
+        torch.amax(flush_rd, dim=0, out=sink)
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    sec = float(np.mean([a.elapsed_time(b) for a, b in evs])) * 1e-3
+    R = int(L.row_offsets[L.G].item())
+    ab = algorithmic_bytes(cfg, R)
+    key = {"layout_noalloc": "layout", "dispatch_layout_nvfp4": None}.get(op, op)
+    nbytes = ab["layout"] + ab["dispatch_nvfp4"] if key is None else ab.get(key)
+    line = {"only": op, "workload": cfg.name, "T": T, "hidden": H, "rows": R, "steps": args.steps,
+            "warmup": args.warmup, "us": sec * 1e6, "algorithmic_bytes": nbytes,
+            "GB/s": nbytes / sec / 1e9 if nbytes else None}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -902,6 +1058,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the per-workload sweep (fused layout + NVFP4 dispatch, combine, step)")
+    ap.add_argument("--only", choices=ONLY_OPS,
+                    help="run one library call alone on --config (for profiling) and print its time")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -910,6 +1068,8 @@ def main():
         cfg = W.scaled(cfg, C=cfg.rerun_C)
     if args.impl == "reference":
         return run_reference(args, cfg)
+    if args.only:
+        return run_only(args, cfg)
     return run_ours(args, cfg)
 
 
