@@ -297,17 +297,32 @@ ep_dispatch_fp8_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int 
 // With `early` set the kernel directly follows the layout kernel of the same call (which let it
 // launch only once every earlier kernel had completed), so phase 1 of the first round runs
 // before waiting for the layout and overlaps it; the layout's outputs are read after the wait.
+// With `write_meta` set the layout kernel left src_info and expert_ids to this kernel: each lane
+// that sends a row also writes that row's (token, slot) and expert, so the layout's critical
+// path carries only row_of.  The metadata is written even when the status word stops the
+// payload, as the layout would have written it.
 // ---------------------------------------------------------------------------------------
 constexpr int kStageSlots = 8;
 constexpr int kStageMaxThreads = 256;
 
+// (token, slot) and expert of row r of token t (slot K: the shared copy).
+__device__ __forceinline__ void write_row_meta(int r, int t, int k, int K, int E,
+                                               const int32_t *__restrict__ ids,
+                                               int32_t *__restrict__ src_info,
+                                               int32_t *__restrict__ expert_ids) {
+    reinterpret_cast<int2 *>(src_info)[r] = make_int2(t, k);
+    expert_ids[r] = k < K ? ids[(size_t)t * K + k] : E;
+}
+
 __global__ void __launch_bounds__(kStageMaxThreads, 4)
 ep_dispatch_nvfp4_staged_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int E, int S, int G,
-                                int R_max, int early, const int32_t *__restrict__ row_of,
+                                int R_max, int early, int write_meta, const int32_t *__restrict__ ids,
+                                const int32_t *__restrict__ row_of,
                                 const int32_t *__restrict__ row_offsets,
                                 const int32_t *__restrict__ status, uint8_t *__restrict__ out_fp4,
                                 uint8_t *__restrict__ out_scales, uint16_t *__restrict__ out_inv,
-                                int32_t *__restrict__ scales_offsets) {
+                                int32_t *__restrict__ scales_offsets, int32_t *__restrict__ src_info,
+                                int32_t *__restrict__ expert_ids) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ __align__(16) float s_red[2][kStageMaxThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -386,12 +401,20 @@ ep_dispatch_nvfp4_staged_kernel(const uint16_t *__restrict__ x, int T, int H, in
             pdl_begin();
             waited = true;
         }
-        if (load_status(status)) return;   // constant per call: no copy was issued before
+        const int shared_base = S ? row_offsets[E] : 0;
+        const int nrows = K + S;
+        if (load_status(status)) {         // constant per call: no copy was issued before
+            if (write_meta)                // no payload, but every row's metadata
+                for (int t = tb + warp; t < te; t += nwarps)
+                    for (int k = lane; k < nrows; k += 32) {
+                        const int r = k < K ? row_of[(size_t)t * K + k] : shared_base + t;
+                        if (r >= 0 && r < R_max) write_row_meta(r, t, k, K, E, ids, src_info, expert_ids);
+                    }
+            return;
+        }
         if (blockIdx.x == 0 && r0 == tb)
             for (int gi = tid; gi <= G; gi += blockDim.x) scales_offsets[gi] = row_offsets[gi];
         // ---- phase 2
-        const int shared_base = S ? row_offsets[E] : 0;
-        const int nrows = K + S;
         for (int j = warp; j < r1 - r0; j += nwarps) {
             const int t = r0 + j;
             const unsigned char *slotp = s_stage + (size_t)j * slot_bytes;
@@ -401,6 +424,7 @@ ep_dispatch_nvfp4_staged_kernel(const uint16_t *__restrict__ x, int T, int H, in
                 bulk_store(out_fp4 + (size_t)r * code_bytes, slotp, code_bytes);
                 bulk_store(out_scales + (size_t)r * scale_bytes, slotp + code_bytes, scale_bytes);
                 out_inv[r] = s_inv[j];
+                if (write_meta) write_row_meta(r, t, k, K, E, ids, src_info, expert_ids);
             }
         }
         bulk_commit();
@@ -411,14 +435,11 @@ ep_dispatch_nvfp4_staged_kernel(const uint16_t *__restrict__ x, int T, int H, in
     bulk_wait_all();                // every copy of this thread has landed
 }
 
-// Staged dispatch on as many CTAs as fit, when each CTA's tokens fit two rounds of staging
-// slots; -1 when the shape does not suit it.
-inline int launch_nvfp4_staged(const uint16_t *x, int H, const ep_layout_t *L, uint8_t *out_fp4,
-                               uint8_t *out_scales, uint16_t *out_inv, int32_t *scales_offsets,
-                               int early, int busy_sms, cudaStream_t st) {
-    const int T = L->T;
-    if (T == 0 || H % 256 != 0 || H / 32 > kStageMaxThreads) return -1;
-    const int threads = max(H / 32, 32 * ((L->K + 1 + 31) / 32));
+// Grid of the staged dispatch (as many CTAs as fit on the SMs the layout leaves free), when
+// each CTA's tokens fit two rounds of staging slots; -1 when the shape does not suit it.
+inline int staged_grid(int T, int K, int H, int busy_sms) {
+    if (T <= 0 || H % 256 != 0 || H / 32 > kStageMaxThreads) return -1;
+    const int threads = max(H / 32, 32 * ((K + 1 + 31) / 32));
     if (threads > kStageMaxThreads) return -1;
     const size_t smem = (size_t)kStageSlots * ((size_t)H / 2 + H / 16) + 2 * kStageSlots;
     if (smem > 48 * 1024 &&
@@ -429,10 +450,8 @@ inline int launch_nvfp4_staged(const uint16_t *x, int H, const ep_layout_t *L, u
     }
     int grid = resident_blocks(ep_dispatch_nvfp4_staged_kernel, threads, smem);
     if (grid <= 0) return -1;
-    int dev = 0, sms = 0;
-    if (busy_sms > 0 && cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > busy_sms)
-        grid = grid / sms * (sms - busy_sms);   // only the SMs the layout leaves free
+    const int sms = device_sm_count();
+    if (busy_sms > 0 && sms > busy_sms) grid = grid / sms * (sms - busy_sms);   // the SMs left free
     if (grid <= 0) return -1;
     if (grid > T) grid = T;
     const int tpc = (T + grid - 1) / grid;   // the most tokens a CTA gets
@@ -441,12 +460,24 @@ inline int launch_nvfp4_staged(const uint16_t *x, int H, const ep_layout_t *L, u
     // (32,768 tokens at H = 7168) took 304 us staged against 274 us per token, while 16 tokens
     // per CTA (16,384 at H = 4096) took 41 us staged against 48 us.
     if (tpc > 2 * kStageSlots) return -1;
+    return grid;
+}
+
+// The staged dispatch on `grid` CTAs (from staged_grid); with write_meta it also writes the
+// layout's src_info and expert_ids (the layout kernel before it left them out).
+inline int launch_nvfp4_staged(int grid, const uint16_t *x, int H, const int32_t *ids,
+                               const ep_layout_t *L, uint8_t *out_fp4, uint8_t *out_scales,
+                               uint16_t *out_inv, int32_t *scales_offsets, int early, int write_meta,
+                               cudaStream_t st) {
+    const int threads = max(H / 32, 32 * ((L->K + 1 + 31) / 32));
+    const size_t smem = (size_t)kStageSlots * ((size_t)H / 2 + H / 16) + 2 * kStageSlots;
     const int G = L->E + L->fused_shared;
     const int R_max = layout_rows(L);
-    return launch_pdl(ep_dispatch_nvfp4_staged_kernel, dim3(grid), dim3(threads), smem, st, x, T, H,
-                      L->K, L->E, L->fused_shared, G, R_max, early, (const int32_t *)L->row_of,
-                      (const int32_t *)L->row_offsets, (const int32_t *)L->status, out_fp4, out_scales,
-                      out_inv, scales_offsets);
+    return launch_pdl(ep_dispatch_nvfp4_staged_kernel, dim3(grid), dim3(threads), smem, st, x, L->T, H,
+                      L->K, L->E, L->fused_shared, G, R_max, early, write_meta, ids,
+                      (const int32_t *)L->row_of, (const int32_t *)L->row_offsets,
+                      (const int32_t *)L->status, out_fp4, out_scales, out_inv, scales_offsets,
+                      L->src_info, L->expert_ids);
 }
 
 __global__ void ep_cvt_kernel(const float *__restrict__ in, uint8_t *__restrict__ codes, long n, int e4m3) {
@@ -538,16 +569,27 @@ extern "C" int ep_dispatch_layout_nvfp4(const int32_t *topk_ids, int T, int K, i
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return EP_ERR_INVALID_ARG;
     cudaStream_t st = as_stream(stream);
-    int layout_sms = 0;
-    int rc = launch_layout(topk_ids, T, K, n_experts, n_parts, capacity, fused_shared, 1, 0, L, st,
-                           &layout_sms);
-    if (rc != EP_OK) return rc;
     // The dispatch kernel directly follows the layout kernel, which lets it launch only once
     // every earlier kernel of the stream has completed, so its CTAs read and quantise their
     // tokens while the layout is still running and wait for the layout only before storing.
-    rc = launch_nvfp4_staged(input_tokens, H, L, out_fp4, out_scales, out_rowwise_inv_scale,
-                             scales_offsets, 1, layout_sms, st);
-    if (rc != -1) return rc;
+    // When the layout takes the single-cluster kernel and the staged dispatch follows it, the
+    // dispatch can write src_info and expert_ids itself, which takes them off the layout's
+    // critical path.  That pays where the token rows are short for their routed slots
+    // (2H <= 512 K bytes), so the layout, not the read of x, decides when the stores can start:
+    // on GB300 the Qwen3-like step (H = 2048, K = 8) got 1.0 us faster (78.9 -> 78.0 us), while
+    // the DSv3-like (H = 7168, K = 8) and Mixtral-like (H = 4096, K = 2) steps, whose dispatch
+    // is bound by HBM, got 0.8 us slower from the extra scattered stores.
+    const int planned_sms = layout_cluster_plan(T, K, n_experts, n_parts);
+    const int grid = staged_grid(T, K, H, planned_sms);
+    const int meta_in_dispatch = grid > 0 && planned_sms > 0 && 2 * H <= 512 * K;
+    int layout_sms = 0;
+    int rc = launch_layout(topk_ids, T, K, n_experts, n_parts, capacity, fused_shared, 1, 0, L, st,
+                           &layout_sms, meta_in_dispatch ? 0 : 1);
+    if (rc != EP_OK) return rc;
+    if (grid > 0)
+        return launch_nvfp4_staged(grid, input_tokens, H, topk_ids, L, out_fp4, out_scales,
+                                   out_rowwise_inv_scale, scales_offsets, 1,
+                                   meta_in_dispatch && layout_sms > 0, st);
     return launch_nvfp4(input_tokens, H, L, out_fp4, out_scales, out_rowwise_inv_scale,
                         scales_offsets, 1, st);
 }

@@ -148,10 +148,16 @@ inline int resident_blocks(K kernel, int threads, size_t smem) {
 
 // Enqueues a dispatch layout (ep_layout.cu) with groups padded to a multiple of `pad` and at
 // most `row_capacity` rows (0: the default R_max).  *cluster_ctas_used receives the number of
-// SMs the single-cluster layout kernel occupies, or 0 when the two-kernel path ran.
+// SMs the single-cluster layout kernel occupies, or 0 when the two-kernel path ran.  With
+// write_rows 0 an unpadded, uncapped layout that takes the single-cluster kernel leaves
+// src_info and expert_ids unwritten: the dispatch kernel enqueued right after it writes them.
 int launch_layout(const int32_t *topk_ids, int T, int K, int E, int P, int capacity, int S,
                   int pad, int row_capacity, ep_layout_t *L, cudaStream_t st,
-                  int *cluster_ctas_used);
+                  int *cluster_ctas_used, int write_rows = 1);
+
+// SMs the single-cluster layout kernel would occupy for these sizes, or 0 when the layout
+// would take the two-kernel path.
+int layout_cluster_plan(int T, int K, int E, int P);
 
 // Enqueues the routing-map -> compact ids conversion (ep_routing.cu); arguments checked.
 int launch_map_to_topk(const uint8_t *routing_map, const float *dense_probs, int T, int E, int K,

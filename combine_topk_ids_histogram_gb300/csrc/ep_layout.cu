@@ -459,13 +459,17 @@ ep_layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int 
 //   D. after the wait every read is local: cluster totals -> row_offsets (a block scan), counts
 //      of the CTAs before this one -> this CTA's first row per expert; then row_of in flat order,
 //      and src_info / expert_ids from the staging area as contiguous runs.
-// One launch, one cluster barrier after start-up, no global scratch, atomics or fences.
+// One launch, one cluster barrier after start-up, no global scratch, atomics or fences.  A CTA
+// holds up to kClMaxIds ids, so one cluster lays out up to 262,144 (token, slot) pairs.  When
+// the NVFP4 dispatch of the same call writes src_info and expert_ids (write_rows 0), the
+// staging and its copy-out are skipped and only row_of is written in phase D.
 // ---------------------------------------------------------------------------------------
 constexpr int kClThreads = 1024;
 constexpr int kClWarps = kClThreads / 32;
 static_assert(kClWarps == 32, "the cluster kernel scans per-warp values with one warp");
 constexpr int kClMaxCtas = 16;            // largest cluster (non-portable; 8 where 16 is refused)
-constexpr int kClMaxIds = 8192;           // ids of one CTA's range held in shared memory
+constexpr int kClMaxIds = 16384;          // ids of one CTA's range held in shared memory
+constexpr int kClIdBatch = 8;             // ids a lane requests before using the first
 constexpr int kClIdsPerCta = 2048;        // below this many ids per CTA, use fewer CTAs
 static_assert(kMaxE <= kClThreads, "the cluster kernel gives one thread to each expert");
 constexpr size_t kClMaxSmem = 216 * 1024;   // dynamic; leaves room for the static arrays
@@ -553,7 +557,7 @@ __device__ __forceinline__ void cluster_sync_all() {
 __global__ void __launch_bounds__(kClThreads, 1)
 ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int P, int C, int S,
                          int pad, int row_limit, int tile_t, int nbits, unsigned long long per_magic,
-                         unsigned long long k_magic, int32_t *__restrict__ row_offsets,
+                         unsigned long long k_magic, int write_rows, int32_t *__restrict__ row_offsets,
                          int32_t *__restrict__ expert_ids, int32_t *__restrict__ src_info,
                          int32_t *__restrict__ row_of, int32_t *__restrict__ part_tokens,
                          int32_t *__restrict__ status) {
@@ -593,37 +597,38 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
     int *hist = s_whist + warp * EP;
     {
         int bad = 0;
-        // the warp's own run, so its histogram needs no second pass over shared memory; all of
-        // a lane's ids (at most kClMaxIds / kClThreads) are requested before the first is used
-        constexpr int kIdsPerLane = kClMaxIds / kClThreads;
-        static_assert(kIdsPerLane * kClThreads == kClMaxIds, "whole ids per lane");
-        int idv[kIdsPerLane];
-#pragma unroll
-        for (int j = 0; j < kIdsPerLane; ++j) {
-            const int i = w0 + lane + 32 * j;
-            idv[j] = i < w1 ? ids[(size_t)t0 * K + i] : -1;
-        }
+        // the warp's own run, so its histogram needs no second pass over shared memory; a
+        // lane's ids are requested kClIdBatch at a time before the first of them is used (one
+        // batch covers up to 8192 ids per CTA)
         int tk = (w0 + lane) / K, kk = (w0 + lane) - tk * K;
         const int step_t = 32 / K, step_k = 32 - step_t * K;
+        for (int i0 = w0 + lane; i0 < w1; i0 += 32 * kClIdBatch) {
+            int idv[kClIdBatch];
 #pragma unroll
-        for (int j = 0; j < kIdsPerLane; ++j) {
-            const int i = w0 + lane + 32 * j;
-            if (i >= w1) break;
-            int id = idv[j];
-            if (bad_id(id, E)) {
-                bad = 1;
-                id = -1;
+            for (int j = 0; j < kClIdBatch; ++j) {
+                const int i = i0 + 32 * j;
+                idv[j] = i < w1 ? ids[(size_t)t0 * K + i] : -1;
             }
-            s_ids[i] = id;
-            if (id >= 0) {
-                atomicAdd(&hist[id], 1);
-                if (masks) atomicOr(&s_tokmask[tk], (int)(1u << div_magic((unsigned)id, per_magic)));
-            }
-            tk += step_t;
-            kk += step_k;
-            if (kk >= K) {
-                kk -= K;
-                ++tk;
+#pragma unroll
+            for (int j = 0; j < kClIdBatch; ++j) {
+                const int i = i0 + 32 * j;
+                if (i >= w1) break;
+                int id = idv[j];
+                if (bad_id(id, E)) {
+                    bad = 1;
+                    id = -1;
+                }
+                s_ids[i] = id;
+                if (id >= 0) {
+                    atomicAdd(&hist[id], 1);
+                    if (masks) atomicOr(&s_tokmask[tk], (int)(1u << div_magic((unsigned)id, per_magic)));
+                }
+                tk += step_t;
+                kk += step_k;
+                if (kk >= K) {
+                    kk -= K;
+                    ++tk;
+                }
             }
         }
         if (bad) s_bad = 1;
@@ -687,14 +692,14 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
     //    expert's local list (equal-id lanes by ballots), and its staging at that expert-major
     //    local position (flat index in the low bits, expert in the high bits).  s_ids keeps
     //    (local rank << 10 | expert) for the rows written after the wait.
-    {
+    if (write_rows) {
         int tot_l;
         const int v = tid < E ? s_hist[tid] : 0;
         const int ex = block_exclusive_scan_1024(v, s_warp2, tot_l);
         if (tid < E) s_locoff[tid] = ex;
         if (tid == 0) s_nvalid = tot_l;
+        __syncthreads();
     }
-    __syncthreads();
     {
         const unsigned lt_mask = (1u << lane) - 1u;
         for (int base = w0; base < w1; base += 32) {
@@ -707,7 +712,7 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
             if (id >= 0 && lane == __ffs(peers) - 1) hist[id] += __popc(peers);
             __syncwarp();
             if (id >= 0) {
-                s_stage[s_locoff[id] + local] = (id << 16) | i;
+                if (write_rows) s_stage[s_locoff[id] + local] = (id << 16) | i;
                 s_ids[i] = (local << 10) | id;
             }
         }
@@ -743,13 +748,13 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
     }
     int routed;
     const int excl = block_exclusive_scan_1024(ext, s_warp, routed);   // ends with a barrier
-    const int n_valid = s_nvalid;
+    const int n_valid = write_rows ? s_nvalid : 0;
     const int shared_ext = S ? (pad > 1 ? (T + pad - 1) / pad * pad : T) : 0;
     if (tid < E) {
         if (crank == 0) row_offsets[tid] = excl;
         s_first[tid] = excl + before;
         // padding rows of expert tid, spread over the cluster's CTAs
-        for (int r = excl + total + crank; r < excl + ext && r < row_limit; r += ncta) {
+        for (int r = excl + total + crank; write_rows && r < excl + ext && r < row_limit; r += ncta) {
             reinterpret_cast<int2 *>(src_info)[r] = make_int2(-1, -1);
             expert_ids[r] = tid;
         }
@@ -774,7 +779,7 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
         }
         row_of[(size_t)t0 * K + i] = row;
     }
-    for (int j = tid; j < n_valid; j += kClThreads) {
+    for (int j = tid; write_rows && j < n_valid; j += kClThreads) {
         const int v = s_stage[j];
         const int e = v >> 16, i = v & 0xffff;
         if (e < 0 || e >= E || i >= n) continue;   // only a layout raced by a writer of ids
@@ -784,7 +789,7 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
         reinterpret_cast<int2 *>(src_info)[row] = make_int2(t0 + tk, i - tk * K);
         expert_ids[row] = e;
     }
-    if (S) {
+    if (S && write_rows) {
         for (int t = t0 + tid; t < t1 && routed + t < row_limit; t += kClThreads) {
             reinterpret_cast<int2 *>(src_info)[routed + t] = make_int2(t, K);
             expert_ids[routed + t] = E;
@@ -839,10 +844,12 @@ inline int max_cluster_ctas() {
 }
 
 // The whole layout as one cluster of CTAs (see ep_layout_cluster_kernel).  Returns -1 when the
-// sizes do not fit one cluster (the caller then uses the two-kernel path).
+// sizes do not fit one cluster (the caller then uses the two-kernel path).  With write_rows 0
+// (unpadded layouts only) the kernel writes row_offsets, row_of, part_tokens and the status but
+// leaves src_info and expert_ids to the dispatch kernel that follows it.
 inline int launch_cluster_layout(const int32_t *ids, int T, int K, int E, int P, int C, int S,
                                  int pad, int row_limit, ep_layout_t *L, cudaStream_t st,
-                                 int *ctas_used) {
+                                 int *ctas_used, int write_rows = 1) {
     const int max_ctas = max_cluster_ctas();
     if (max_ctas == 0) return -1;   // the two-kernel path needs no shared-memory opt-in
     const int ncta = cluster_ctas(T, K, E, P, max_ctas);
@@ -866,7 +873,7 @@ inline int launch_cluster_layout(const int32_t *ids, int T, int K, int E, int P,
     cfg.numAttrs = 2;
     return launch_result(cudaLaunchKernelEx(&cfg, ep_layout_cluster_kernel, ids, T, K, E, P, C, S,
                                             pad, row_limit, tile_t, key_bits(E + 1), magic_of(E / P),
-                                            magic_of(K),
+                                            magic_of(K), write_rows,
                                             L->row_offsets, L->expert_ids, L->src_info, L->row_of,
                                             L->part_tokens, L->status));
 }
@@ -914,11 +921,17 @@ extern "C" size_t ep_layout_workspace_bytes(int T, int K, int n_experts, int fus
 
 namespace ep {
 
+int layout_cluster_plan(int T, int K, int E, int P) {
+    if (!sizes_ok(T, K, E, 0) || P < 1 || P > E || E % P != 0) return 0;
+    const int max_ctas = max_cluster_ctas();
+    return max_ctas ? cluster_ctas(T, K, E, P, max_ctas) : 0;
+}
+
 // Validates the arguments of a layout call and enqueues it.  *cluster_ctas_used receives the
 // number of SMs the single-cluster kernel occupies (0 when the two-kernel path ran).
 int launch_layout(const int32_t *topk_ids, int T, int K, int E, int P, int capacity, int S,
                   int pad, int row_capacity, ep_layout_t *L, cudaStream_t st,
-                  int *cluster_ctas_used) {
+                  int *cluster_ctas_used, int write_rows) {
     if (cluster_ctas_used) *cluster_ctas_used = 0;
     if (!L || !sizes_ok(T, K, E, S) || !padding_ok(T, K, E, S, pad, row_capacity))
         return EP_ERR_INVALID_ARG;
@@ -946,7 +959,7 @@ int launch_layout(const int32_t *topk_ids, int T, int K, int E, int P, int capac
 
     int used = 0;
     const int rc_cl = launch_cluster_layout(topk_ids, T, K, E, P, capacity, S, pad, row_limit, L,
-                                            st, &used);
+                                            st, &used, pad > 1 || row_capacity > 0 ? 1 : write_rows);
     if (rc_cl != -1) {
         if (cluster_ctas_used) *cluster_ctas_used = used;
         return rc_cl;

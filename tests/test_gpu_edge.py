@@ -137,15 +137,18 @@ def test_ragged_last_tile_of_one_token(ep):
     full_check(ep, ids, x, p, y, 64, P=8)
 
 
-def test_layout_beyond_one_cluster(ep):
-    """T*K above what one thread-block cluster holds: the two-kernel layout (tile histograms,
-    scan by the last CTA, ranks) runs instead of the single-cluster one."""
-    ids, x, p, y = rand_case(17000, 8, 64, 16, 15, unused=0.03)
+@pytest.mark.parametrize("T", [17000, 34000])
+def test_layout_beyond_one_cluster(ep, T):
+    """17,000 tokens (136,000 ids): the single-cluster layout with more than 8192 ids per CTA,
+    each lane's ids loaded in two batches.  34,000 tokens (272,000 ids): above what one
+    thread-block cluster holds, so the two-kernel layout (tile histograms, scan by the last CTA,
+    ranks) runs instead."""
+    ids, x, p, y = rand_case(T, 8, 64, 16, 15, unused=0.03)
     ids[5, 3] = 64                     # one bad id: flagged, then nothing written
     ref = full_check(ep, ids, x, p, y, 64, P=4, S=1)
     assert ref.status == oracle.BAD_EXPERT
     ids[5, 3] = 7
-    full_check(ep, ids, x, p, y, 64, P=4, C=15000, S=1)
+    full_check(ep, ids, x, p, y, 64, P=4, C=T - 2000, S=1)
 
 
 def test_bad_expert_ids_write_nothing(ep):

@@ -138,8 +138,12 @@ def test_random_fused_call_and_routing_map(ep, seed):
     ep.dispatch_layout_nvfp4(dev(ids), dev_bf16(x), E, P, C, bool(S), out_layout=L, out=out)
     assert ep.read_status(L) == ref.status
     assert np.array_equal(L.row_offsets.cpu().numpy(), ref.row_offsets)
+    assert np.array_equal(L.part_tokens.cpu().numpy(), ref.part_tokens)
     assert np.array_equal(L.row_of.cpu().numpy(), ref.row_of)
-    assert np.array_equal(L.src_info.cpu().numpy()[:ref.R], ref.src_info[:ref.R])
+    si, ei = L.src_info.cpu().numpy(), L.expert_ids.cpu().numpy()
+    assert np.array_equal(si[:ref.R], ref.src_info[:ref.R])
+    assert np.array_equal(ei[:ref.R], ref.expert_ids[:ref.R])
+    assert (si[ref.R:Rm] == CANARY32).all() and (ei[ref.R:Rm] == CANARY32).all()
     rfp4, rsc, rinv, _ = oracle.dispatch_nvfp4(x, ref, fill=0xA5)
     assert np.array_equal(out[0].cpu().numpy(), rfp4)
     assert np.array_equal(out[1].cpu().numpy(), rsc)

@@ -144,9 +144,11 @@ def test_padded_parity(ep, name, T, H, pad, capmode):
     assert ref.status == 0 and (ref.src_info[:ref.R, 0] < 0).any()   # padding rows exercised
 
 
-def test_padded_layout_beyond_one_cluster(ep):
-    """Enough ids for the two-kernel layout path (more than one thread-block cluster holds)."""
-    cfg = W.scaled(W.CONFIGS["dsv3"], T=20000, H=256, C=20000)
+@pytest.mark.parametrize("T", [20000, 34000])
+def test_padded_layout_beyond_one_cluster(ep, T):
+    """160,000 ids: the single-cluster layout with two id batches per lane; 272,000 ids: more
+    than one thread-block cluster holds, so the two-kernel layout runs."""
+    cfg = W.scaled(W.CONFIGS["dsv3"], T=T, H=256, C=T)
     run_all(ep, cfg, 64, None)
 
 
@@ -192,7 +194,8 @@ EDGE = [  # T, K, E, S, P, pad, case
     (129, 1, 1, 0, 1, 3, "one expert, one slot"),
     (200, 3, 8, 1, 2, 8, "every slot unused"),
     (257, 4, 3, 1, 1, 5, "duplicate ids"),
-    (17000, 8, 64, 1, 4, 16, "a bad id, two-kernel layout"),
+    (17000, 8, 64, 1, 4, 16, "a bad id, single-cluster layout, two id batches"),
+    (34000, 8, 64, 1, 4, 16, "a bad id, two-kernel layout"),
 ]
 
 

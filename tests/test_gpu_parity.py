@@ -135,6 +135,7 @@ def test_layout_reuse_across_calls(ep):
 FUSED_CASES = [("tiny", None, None, None), ("dsv3", 900, None, None), ("qwen3", 1500, None, None),
                ("dsv3", 7000, 7000, None),      # more tokens per CTA than staging slots: rounds
                ("dsv3_large", 1000, 610, None),  # capacity overflow: nothing written
+               ("qwen3", 1500, 100, None),       # overflow where the dispatch writes the metadata
                ("mixtral", 3000, None, 784),    # H not a multiple of 256: the per-token kernel
                ("mixtral", 90000, None, 256)]   # beyond two rounds per CTA: the per-token kernel
 

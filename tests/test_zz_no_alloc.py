@@ -53,7 +53,7 @@ def _check_against_oracle(got, ids, E, P, C, S):
 
 @pytest.mark.parametrize("T,K,E,P,S,C", [
     (4096, 8, 256, 8, True, 4096),        # the DSv3-shaped layer: fits one cluster, no scratch
-    (30001, 8, 256, 8, False, 30001),     # 240,008 ids: the fixed scratch array, ragged tiles
+    (40001, 8, 256, 8, False, 40001),     # 320,008 ids: the fixed scratch array, ragged tiles
 ])
 def test_noalloc_layout_equals_allocating_layout_on_two_calls(T, K, E, P, S, C):
     import combine_topk_ids_histogram_gb300 as ep
@@ -82,7 +82,7 @@ def test_noalloc_layout_error_then_clean_call():
     the shared array is left ready for the next call whatever the status."""
     import combine_topk_ids_histogram_gb300 as ep
 
-    T, K, E, P, S = 32768, 8, 256, 8, True              # 262,144 ids: the fixed scratch array
+    T, K, E, P, S = 40000, 8, 256, 8, True              # 320,000 ids: the fixed scratch array
     out = _no_workspace_layout(ep, T, K, E, P, S)
     ids_h = _routing(T, K, E, 7)
     bad = ids_h.copy()
