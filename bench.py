@@ -1060,6 +1060,8 @@ def main():
                     help="skip the per-workload sweep (fused layout + NVFP4 dispatch, combine, step)")
     ap.add_argument("--only", choices=ONLY_OPS,
                     help="run one library call alone on --config (for profiling) and print its time")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="with --only: the workload's recipe at this many tokens")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -1069,6 +1071,8 @@ def main():
     if args.impl == "reference":
         return run_reference(args, cfg)
     if args.only:
+        if args.tokens:
+            cfg = W.scaled(cfg, T=args.tokens, C=max(cfg.capacity, args.tokens) if cfg.C else None)
         return run_only(args, cfg)
     return run_ours(args, cfg)
 
