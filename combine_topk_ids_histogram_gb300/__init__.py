@@ -19,7 +19,10 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libep_gb300.so")
+# EP_GB300_CHECKED=1 selects the bounds-checked debug build of the same sources, which reports
+# an index outside its buffer as EP_STATUS_BOUNDS instead of relying on the caller's layout.
+CHECKED = os.environ.get("EP_GB300_CHECKED", "0") == "1"
+LIB_PATH = os.path.join(_HERE, "_build", "libep_gb300_checked.so" if CHECKED else "libep_gb300.so")
 
 EP_OK = 0
 EP_ERR_INVALID_ARG = 1
@@ -27,9 +30,11 @@ EP_ERR_OVERFLOW = 2
 EP_ERR_BAD_EXPERT = 3
 EP_ERR_CUDA = 5
 EP_ERR_TOO_LARGE = 6
+EP_ERR_BOUNDS = 7
 NOALLOC_WORKSPACE_BYTES = 1 << 20
 STATUS_OVERFLOW = 1
 STATUS_BAD_EXPERT = 2
+STATUS_BOUNDS = 8
 
 
 class EPError(RuntimeError):

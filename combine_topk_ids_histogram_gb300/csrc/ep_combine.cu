@@ -58,7 +58,7 @@ ep_combine_kernel(const uint16_t *__restrict__ y, const float *__restrict__ prob
         } else if (tid == K && S) {
             r = shared_base + tt;
         }
-        if (r >= R_max) r = -1;
+        if (!row_ok(r, R_max, status)) r = -1;
     };
 
     int t = blockIdx.x;
@@ -136,8 +136,9 @@ ep_combine_bwd_kernel(const uint16_t *__restrict__ g, const uint16_t *__restrict
     pdl_wait();
     if (load_status(status)) return;
     if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: zero gradient rows
-        fill_group_padding(blockIdx.x / fparts, blockIdx.x % fparts, fparts, pad, row_offsets, src_info,
-                           PadFill{grad_y, 2 * H, 0u}, PadFill{nullptr, 0, 0u}, PadFill{nullptr, 0, 0u});
+        fill_group_padding(blockIdx.x / fparts, blockIdx.x % fparts, fparts, pad, R_max, row_offsets,
+                           src_info, status, PadFill{grad_y, 2 * H, 0u}, PadFill{nullptr, 0, 0u},
+                           PadFill{nullptr, 0, 0u});
         return;
     }
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -149,7 +150,7 @@ ep_combine_bwd_kernel(const uint16_t *__restrict__ g, const uint16_t *__restrict
             r = row_of[(size_t)t * K + tid];
             p = probs[(size_t)t * K + tid];
         }
-        s_rows[tid] = (r < R_max) ? r : -1;
+        s_rows[tid] = row_ok(r, R_max, status) ? r : -1;
         s_p[tid] = p;
     }
     __syncthreads();
@@ -162,7 +163,7 @@ ep_combine_bwd_kernel(const uint16_t *__restrict__ g, const uint16_t *__restrict
         dot[k] = 0.0f;
     }
     int shared_row = S ? row_offsets[E] + t : -1;
-    if (shared_row >= R_max) shared_row = -1;
+    if (S && !row_ok(shared_row, R_max, status)) shared_row = -1;
     const int nv = H / 8;
     for (int c = tid; c < nv; c += blockDim.x) {
         const uint4 gv = ld_stream(g + (size_t)t * H + (size_t)c * 8);

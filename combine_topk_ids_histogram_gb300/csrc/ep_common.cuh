@@ -52,6 +52,30 @@ __device__ __forceinline__ int load_status(const int32_t *status) {
 }
 
 // ---------------------------------------------------------------------------------------
+// The bounds-checked debug build (compiled with -DEP_BOUNDS_CHECK=1) checks every index that
+// comes from data against the buffer it indexes, skips an access that fails and sets
+// EP_STATUS_BOUNDS in the layout's status word.  In the default build kBoundsCheck is false
+// and the extra checks compile away.
+// ---------------------------------------------------------------------------------------
+#ifndef EP_BOUNDS_CHECK
+#define EP_BOUNDS_CHECK 0
+#endif
+constexpr bool kBoundsCheck = EP_BOUNDS_CHECK != 0;
+
+// Records a failed check in the status word (checked build only).
+__device__ __forceinline__ void bounds_fail(const int32_t *status) {
+    if (kBoundsCheck) atomicOr(const_cast<int32_t *>(status), EP_STATUS_BOUNDS);
+}
+
+// Whether a row read from a layout may be used.  Both builds skip rows outside [0, R_max)
+// (-1 marks an unused slot); the checked build also records any such row other than -1.
+__device__ __forceinline__ bool row_ok(int r, int R_max, const int32_t *status) {
+    if (r >= 0 && r < R_max) return true;
+    if (r != -1) bounds_fail(status);
+    return false;
+}
+
+// ---------------------------------------------------------------------------------------
 // bf16 <-> fp32.  A 32-bit word holds two bf16: element 2i in the low half.
 // ---------------------------------------------------------------------------------------
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

@@ -64,8 +64,8 @@ ep_dispatch_nvfp4_kernel(const uint16_t *__restrict__ x, int T, int H, int K, in
     if (!early) pdl_wait();
     if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: a group's padding rows
         if (!load_status(status))
-            fill_group_padding_call(blockIdx.x / fparts, blockIdx.x % fparts, fparts, pad, row_offsets,
-                                    src_info, f0, f1, f2);
+            fill_group_padding_call(blockIdx.x / fparts, blockIdx.x % fparts, fparts, pad, R_max,
+                                    row_offsets, src_info, status, f0, f1, f2);
         return;
     }
     const int tid = threadIdx.x;
@@ -134,7 +134,7 @@ ep_dispatch_nvfp4_kernel(const uint16_t *__restrict__ x, int T, int H, int K, in
     const size_t code_bytes = (size_t)H / 2, scale_bytes = (size_t)H / 16;
     for (int k = 0; k < nrows; ++k) {
         const int r = s_rows[k];
-        if (r < 0 || r >= R_max) continue;
+        if (!row_ok(r, R_max, status)) continue;
         uint8_t *dst = out_fp4 + (size_t)r * code_bytes + (size_t)tid * 8 * BPT;
         uint8_t *dsc = out_scales + (size_t)r * scale_bytes + (size_t)tid * BPT;
         if (BPT == 2) {
@@ -159,8 +159,9 @@ ep_dispatch_bf16_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int
     pdl_wait();
     if (load_status(status)) return;
     if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: a group's padding rows
-        fill_group_padding_call(blockIdx.x / fparts, blockIdx.x % fparts, fparts, pad, row_offsets,
-                                src_info, f0, PadFill{nullptr, 0, 0u}, PadFill{nullptr, 0, 0u});
+        fill_group_padding_call(blockIdx.x / fparts, blockIdx.x % fparts, fparts, pad, R_max,
+                                row_offsets, src_info, status, f0, PadFill{nullptr, 0, 0u},
+                                PadFill{nullptr, 0, 0u});
         return;
     }
     const int tid = threadIdx.x;
@@ -182,7 +183,7 @@ ep_dispatch_bf16_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int
         }
         for (int k = 0; k < nrows; ++k) {
             const int r = s_rows[k];
-            if (r < 0 || r >= R_max) continue;
+            if (!row_ok(r, R_max, status)) continue;
             uint16_t *dst = out + (size_t)r * H;
 #pragma unroll
             for (int i = 0; i < kBf16Chunks; ++i) {
@@ -215,8 +216,8 @@ ep_dispatch_fp8_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int 
     pdl_wait();
     if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: a group's padding rows
         if (!load_status(status))
-            fill_group_padding_call(blockIdx.x / fparts, blockIdx.x % fparts, fparts, pad, row_offsets,
-                                    src_info, f0, f1, PadFill{nullptr, 0, 0u});
+            fill_group_padding_call(blockIdx.x / fparts, blockIdx.x % fparts, fparts, pad, R_max,
+                                    row_offsets, src_info, status, f0, f1, PadFill{nullptr, 0, 0u});
         return;
     }
     const int tid = threadIdx.x;
@@ -278,7 +279,7 @@ ep_dispatch_fp8_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int 
     const int nblk = H / kFp8Block;
     for (int k = 0; k < nrows; ++k) {
         const int r = s_rows[k];
-        if (r < 0 || r >= R_max) continue;
+        if (!row_ok(r, R_max, status)) continue;
         uint8_t *dst = out_fp8 + (size_t)r * H;
         if (off1 < H) st_stream(dst + off1, make_uint4(w1[0], w1[1], w1[2], w1[3]));
         if (off2 < H) st_stream(dst + off2, make_uint4(w2[0], w2[1], w2[2], w2[3]));
@@ -408,7 +409,7 @@ ep_dispatch_nvfp4_staged_kernel(const uint16_t *__restrict__ x, int T, int H, in
                 for (int t = tb + warp; t < te; t += nwarps)
                     for (int k = lane; k < nrows; k += 32) {
                         const int r = k < K ? row_of[(size_t)t * K + k] : shared_base + t;
-                        if (r >= 0 && r < R_max) write_row_meta(r, t, k, K, E, ids, src_info, expert_ids);
+                        if (row_ok(r, R_max, status)) write_row_meta(r, t, k, K, E, ids, src_info, expert_ids);
                     }
             return;
         }
@@ -420,7 +421,7 @@ ep_dispatch_nvfp4_staged_kernel(const uint16_t *__restrict__ x, int T, int H, in
             const unsigned char *slotp = s_stage + (size_t)j * slot_bytes;
             for (int k = lane; k < nrows; k += 32) {
                 const int r = k < K ? row_of[(size_t)t * K + k] : shared_base + t;
-                if (r < 0 || r >= R_max) continue;
+                if (!row_ok(r, R_max, status)) continue;
                 bulk_store(out_fp4 + (size_t)r * code_bytes, slotp, code_bytes);
                 bulk_store(out_scales + (size_t)r * scale_bytes, slotp + code_bytes, scale_bytes);
                 out_inv[r] = s_inv[j];

@@ -148,7 +148,8 @@ __device__ __forceinline__ void count_partition_tokens(const int *s_ids, int nto
 // from chunk to chunk by adding 32 with a carry, so there is one division per lane, not per id.
 __device__ __forceinline__ void rank_and_write(const int *s_ids, int w0, int w1, int t0, int K,
                                                int row_limit, int nbits, int *hist, int32_t *row_of,
-                                               int32_t *src_info, int32_t *expert_ids) {
+                                               int32_t *src_info, int32_t *expert_ids,
+                                               const int32_t *status) {
     const int lane = threadIdx.x & 31;
     const unsigned lt_mask = (1u << lane) - 1u;
     int tk = (w0 + lane) / K, kk = (w0 + lane) - tk * K;
@@ -163,7 +164,8 @@ __device__ __forceinline__ void rank_and_write(const int *s_ids, int w0, int w1,
         if (id >= 0 && lane == __ffs(peers) - 1) hist[id] += __popc(peers);
         __syncwarp();
         if (i < w1) {
-            if (row >= row_limit) row = -1;
+            if (kBoundsCheck && id >= 0 && row < 0) bounds_fail(status);
+            if (row >= row_limit || row < 0) row = -1;
             row_of[(size_t)t0 * K + i] = row;
             if (row >= 0) {
                 reinterpret_cast<int2 *>(src_info)[row] = make_int2(t0 + tk, kk);
@@ -365,7 +367,8 @@ ep_layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int 
                       int row_limit, int tile_t, int nTiles, int nbits, int one_wave,
                       const int32_t *__restrict__ cnt,
                       const int32_t *__restrict__ row_offsets, int32_t *__restrict__ row_of,
-                      int32_t *__restrict__ src_info, int32_t *__restrict__ expert_ids) {
+                      int32_t *__restrict__ src_info, int32_t *__restrict__ expert_ids,
+                      const int32_t *__restrict__ status) {
     extern __shared__ int smem[];
     int *s_whist = smem;                       // [kLayoutWarps][E]
     int *s_ids = smem + kLayoutWarps * E;      // [tile_t * K]
@@ -424,7 +427,7 @@ ep_layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int 
         }
     }
     __syncthreads();
-    rank_and_write(s_ids, w0, w1, t0, K, row_limit, nbits, hist, row_of, src_info, expert_ids);
+    rank_and_write(s_ids, w0, w1, t0, K, row_limit, nbits, hist, row_of, src_info, expert_ids, status);
     if (S) {
         const int rs = row_offsets[E];
         for (int t = t0 + tid; t < t1 && rs + t < row_limit; t += blockDim.x) {
@@ -571,6 +574,7 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
     __shared__ int s_warp2[kClWarps + 1];
     __shared__ int s_bad;
     __shared__ int s_nvalid;
+    __shared__ int s_bounds;   // a failed index check of the bounds-checked build
 
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
@@ -590,7 +594,10 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
     for (int i = tid; i < kClWarps * EP; i += kClThreads) s_whist[i] = 0;
     if (masks)
         for (int i = tid; i < ntok; i += kClThreads) s_tokmask[i] = 0;
-    if (tid == 0) s_bad = 0;
+    if (tid == 0) {
+        s_bad = 0;
+        s_bounds = 0;
+    }
     __syncthreads();
     const int per_warp = ((n + kClWarps - 1) / kClWarps + 31) / 32 * 32;
     const int w0 = min(n, warp * per_warp), w1 = min(n, w0 + per_warp);
@@ -712,7 +719,11 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
             if (id >= 0 && lane == __ffs(peers) - 1) hist[id] += __popc(peers);
             __syncwarp();
             if (id >= 0) {
-                if (write_rows) s_stage[s_locoff[id] + local] = (id << 16) | i;
+                if (write_rows) {
+                    const int pos = s_locoff[id] + local;
+                    if (!kBoundsCheck || (pos >= 0 && pos < n)) s_stage[pos] = (id << 16) | i;
+                    else s_bounds = 1;
+                }
                 s_ids[i] = (local << 10) | id;
             }
         }
@@ -774,17 +785,28 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
         const int v = s_ids[i];
         int row = -1;
         if (v >= 0) {
-            row = s_first[v & 1023] + (v >> 10);
-            if (row >= row_limit) row = -1;
+            if (kBoundsCheck && (v & 1023) >= E) {
+                s_bounds = 1;
+            } else {
+                row = s_first[v & 1023] + (v >> 10);
+                if (kBoundsCheck && row < 0) s_bounds = 1;
+                if (row >= row_limit || row < 0) row = -1;
+            }
         }
         row_of[(size_t)t0 * K + i] = row;
     }
     for (int j = tid; write_rows && j < n_valid; j += kClThreads) {
         const int v = s_stage[j];
         const int e = v >> 16, i = v & 0xffff;
-        if (e < 0 || e >= E || i >= n) continue;   // only a layout raced by a writer of ids
+        if (e < 0 || e >= E || i >= n) {   // only a layout raced by a writer of ids
+            if (kBoundsCheck) s_bounds = 1;
+            continue;
+        }
         const int row = s_first[e] + (j - s_locoff[e]);
-        if (row < 0 || row >= row_limit) continue;
+        if (row < 0 || row >= row_limit) {   // at or past the row capacity: not recorded
+            if (kBoundsCheck && row < 0) s_bounds = 1;
+            continue;
+        }
         const int tk = div_magic((unsigned)i, k_magic);
         reinterpret_cast<int2 *>(src_info)[row] = make_int2(t0 + tk, i - tk * K);
         expert_ids[row] = e;
@@ -800,6 +822,11 @@ ep_layout_cluster_kernel(const int32_t *__restrict__ ids, int T, int K, int E, i
             reinterpret_cast<int2 *>(src_info)[r] = make_int2(-1, -1);
             expert_ids[r] = E;
         }
+    }
+    if (kBoundsCheck) {   // after CTA 0 has stored the status word, every CTA adds its failures
+        __syncthreads();
+        cluster_sync_all();
+        if (tid == 0 && s_bounds) bounds_fail(status);
     }
 }
 
@@ -907,7 +934,7 @@ int launch_tiled_layout(const int32_t *topk_ids, int T, int K, int E, int P, int
     return launch_pdl(ep_layout_rank_kernel, dim3(nTiles), dim3(kLayoutThreads), smem_rank, st,
                       topk_ids, T, K, E, S, pad, row_limit, tt, nTiles, key_bits(E + 1), wave,
                       (const int32_t *)ws.cnt, (const int32_t *)L->row_offsets, L->row_of,
-                      L->src_info, L->expert_ids);
+                      L->src_info, L->expert_ids, (const int32_t *)L->status);
 }
 
 }  // namespace
@@ -1013,6 +1040,7 @@ extern "C" int ep_read_status(const ep_layout_t *L, void *stream, int32_t *host_
         return EP_ERR_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return EP_ERR_CUDA;
     *host_status = v;
+    if (v & EP_STATUS_BOUNDS) return EP_ERR_BOUNDS;
     if (v & EP_STATUS_OVERFLOW) return EP_ERR_OVERFLOW;
     if (v & EP_STATUS_BAD_EXPERT) return EP_ERR_BAD_EXPERT;
     return EP_OK;
@@ -1028,6 +1056,8 @@ extern "C" const char *ep_strerror(int code) {
         case EP_ERR_BAD_EXPERT: return "an expert id was outside [-1, n_experts)";
         case EP_ERR_CUDA: return "CUDA error";
         case EP_ERR_TOO_LARGE: return "the sizes need more scratch than the fixed no-allocation array holds";
+        case EP_ERR_BOUNDS:
+            return "an index fell outside its buffer and the access was skipped (bounds-checked build)";
         default: return "unknown error";
     }
 }

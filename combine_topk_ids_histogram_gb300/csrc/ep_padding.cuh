@@ -40,14 +40,20 @@ __device__ __forceinline__ void fill_row(const PadFill &f, int row, int lane) {
 // (every row before it is one of the group's routed rows).  The group's rows are shared by
 // `nparts` CTAs: the whole CTA finds `first`, then its warps write the rows of part `part`
 // (every nparts-th warp-sized step).  Call only while the layout's status word is 0 (then every
-// row is below R_max).
-__device__ __forceinline__ void fill_group_padding(int g, int part, int nparts, int pad,
+// row is below R_max); the bounds-checked build also checks the group's rows against
+// [0, R_max) and records a group outside it instead of filling it.
+__device__ __forceinline__ void fill_group_padding(int g, int part, int nparts, int pad, int R_max,
                                                    const int32_t *__restrict__ row_offsets,
-                                                   const int32_t *__restrict__ src_info, const PadFill &f0,
+                                                   const int32_t *__restrict__ src_info,
+                                                   const int32_t *__restrict__ status, const PadFill &f0,
                                                    const PadFill &f1, const PadFill &f2) {
     __shared__ int s_first;
     const int hi = row_offsets[g + 1];
     const int lo = max(row_offsets[g], hi - (pad - 1));
+    if (kBoundsCheck && (lo < 0 || hi > R_max || lo > hi)) {
+        if (threadIdx.x == 0) bounds_fail(status);
+        return;
+    }
     if (threadIdx.x == 0) s_first = hi;
     __syncthreads();
     for (int r = lo + threadIdx.x; r < hi; r += blockDim.x)
@@ -63,11 +69,12 @@ __device__ __forceinline__ void fill_group_padding(int g, int part, int nparts, 
 
 // The same as a separate function, for kernels whose own register allocation should not
 // carry the fill's.
-static __device__ __noinline__ void fill_group_padding_call(int g, int part, int nparts, int pad,
+static __device__ __noinline__ void fill_group_padding_call(int g, int part, int nparts, int pad, int R_max,
                                                             const int32_t *__restrict__ row_offsets,
                                                             const int32_t *__restrict__ src_info,
+                                                            const int32_t *__restrict__ status,
                                                             PadFill f0, PadFill f1, PadFill f2) {
-    fill_group_padding(g, part, nparts, pad, row_offsets, src_info, f0, f1, f2);
+    fill_group_padding(g, part, nparts, pad, R_max, row_offsets, src_info, status, f0, f1, f2);
 }
 
 // CTAs sharing one group's padding rows, for CTAs of `threads` threads: enough for about eight

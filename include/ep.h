@@ -52,13 +52,24 @@ typedef enum {
                                  or the rows exceed the layout's row capacity             */
     EP_ERR_BAD_EXPERT = 3,    /* ep_read_status: an expert id was outside [-1, E)            */
     EP_ERR_CUDA = 5,          /* a CUDA call failed (launch error, or the sync in read_status) */
-    EP_ERR_TOO_LARGE = 6      /* ep_dispatch_layout_noalloc: the sizes need more scratch than
+    EP_ERR_TOO_LARGE = 6,     /* ep_dispatch_layout_noalloc: the sizes need more scratch than
                                  its fixed array holds (EP_NOALLOC_WORKSPACE_BYTES)            */
+    EP_ERR_BOUNDS = 7         /* ep_read_status, bounds-checked build only: an index fell
+                                 outside its buffer and the access was skipped                */
 } ep_status_t;
 
 /* Bits of the device status word written by ep_dispatch_layout. */
 #define EP_STATUS_OVERFLOW   1
 #define EP_STATUS_BAD_EXPERT 2
+/*
+ * Set only by the bounds-checked debug build of the library (libep_gb300_checked.so, compiled
+ * with EP_BOUNDS_CHECK=1).  That build checks every index that comes from data against the
+ * buffer it indexes: a row read from a layout (row_of, row_offsets) against [0, R_max), where
+ * -1 marks an unused slot, and a position computed inside the layout kernel against its
+ * shared-memory range.  An access that fails is skipped, not performed, and this bit is set.
+ * The default build skips rows outside [0, R_max) in the same way but records nothing.
+ */
+#define EP_STATUS_BOUNDS     8
 
 /*
  * The dispatch layout: caller-allocated device buffers, filled by ep_dispatch_layout and read
@@ -317,8 +328,9 @@ int ep_dispatch_bwd(const uint16_t *grad_rows, int hidden_size, const ep_layout_
 
 /*
  * ep_read_status -- synchronise `stream` and copy the layout's status word to *host_status.
- * Returns EP_OK, EP_ERR_OVERFLOW or EP_ERR_BAD_EXPERT (overflow reported first when both bits
- * are set), or EP_ERR_CUDA.  The one call of this library that blocks the host.
+ * Returns EP_OK, EP_ERR_BOUNDS (bounds-checked build only; reported first), EP_ERR_OVERFLOW or
+ * EP_ERR_BAD_EXPERT (overflow reported before a bad expert id when both bits are set), or
+ * EP_ERR_CUDA.  The one call of this library that blocks the host.
  */
 int ep_read_status(const ep_layout_t *L, void *stream, int32_t *host_status);
 

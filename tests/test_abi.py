@@ -18,6 +18,11 @@ def libpath():
     return entry._load_builder().build()
 
 
+@pytest.fixture(scope="module")
+def checked_libpath():
+    return entry._load_builder().build(checked=True)
+
+
 def declared_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
@@ -40,6 +45,19 @@ def test_library_exports_every_declared_symbol(libpath):
     lib = ctypes.CDLL(libpath)
     for n in declared_functions():
         assert getattr(lib, n) is not None
+
+
+def test_checked_build_exports_the_same_symbols(libpath, checked_libpath):
+    """The bounds-checked debug build is the same ABI."""
+    def exported(path):
+        out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                             check=True).stdout
+        return set(re.findall(r"\bT (ep_[a-z0-9_]+)$", out, flags=re.M))
+    assert exported(checked_libpath) == exported(libpath)
+    assert set(declared_functions()) <= exported(checked_libpath)
+    lib = ctypes.CDLL(checked_libpath)
+    lib.ep_strerror.restype = ctypes.c_char_p
+    assert b"bounds" in lib.ep_strerror(7)
 
 
 def test_binding_signatures_cover_the_header(libpath):

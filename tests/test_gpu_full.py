@@ -144,6 +144,7 @@ def run_full(ep, cfg, C=None, backward=False, bf16=False):
         assert (out.view(torch.int16) == FILL16 - 65536).all(), "combine wrote on overflow"
         return ref
     check_combine_full(out, y_host, probs, ref, f"{cfg.name} combine")
+    assert torch.equal(ep.combine(yd, pd, L).view(torch.int16), out.view(torch.int16)), "combine rerun"
     if bf16:
         rows = filled((R_max, H), FILL16, torch.int16).view(torch.bfloat16)
         ep.dispatch_bf16(xd, L, out=rows)
@@ -162,11 +163,17 @@ def run_full(ep, cfg, C=None, backward=False, bf16=False):
             assert_close_bf16(gyh[a:b], rgy64[a:b], f"{cfg.name} grad_y rows {a}..{b}")
         assert np.array_equal(gyh[R:], rgy[R:]), "grad_y rows past R were written"
         assert_close_gradp(gp.cpu().numpy(), rgp, abs_dots(g, y_host, ref.row_of), f"{cfg.name} grad_p")
-        del gyh, rgy, rgy64
+        # determinism: a second call gives the same bytes (grad_p's reduction order is fixed)
+        gy2, gp2 = ep.combine_bwd(dev_bf16(g), yd, pd, L)
+        assert torch.equal(gy2[:R].view(torch.int16), gy[:R].view(torch.int16))
+        assert torch.equal(gp2.view(torch.int32), gp.view(torch.int32))
+        del gyh, rgy, rgy64, gy2, gp2
         gr = W.make_grad_rows(cfg)
         gx = filled((T, H), FILL16, torch.int16).view(torch.bfloat16)
-        ep.dispatch_bwd(dev_bf16(gr), L, out=gx)
+        grd = dev_bf16(gr)
+        ep.dispatch_bwd(grd, L, out=gx)
         check_combine_full(gx, gr, probs, ref, f"{cfg.name} dispatch backward", weighted=False)
+        assert torch.equal(ep.dispatch_bwd(grd, L).view(torch.int16), gx.view(torch.int16))
     return ref
 
 
