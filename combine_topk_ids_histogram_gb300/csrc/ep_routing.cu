@@ -156,6 +156,58 @@ ep_indices_to_multihot_kernel(const int32_t *__restrict__ ids, const float *__re
     }
 }
 
+// Compact -> map when E % 16 == 0 (map rows 16-byte aligned, dense rows 64-byte aligned): each
+// warp builds its token's map and dense rows in shared memory, then writes them with 16-byte
+// stores.  The K slots are broadcast once (id and probability); each lane holding a slot keeps
+// the sum, in ascending slot order, of the probabilities of the slots naming its expert, and
+// the lowest such slot writes it.  About 2K shuffles and a few vector accesses per lane and
+// token, against E/32 * K shuffle pairs in the kernel above.
+__global__ void __launch_bounds__(kRoutingThreads)
+ep_indices_to_multihot_wide_kernel(const int32_t *__restrict__ ids, const float *__restrict__ probs, int T,
+                                   int K, int E, uint8_t *__restrict__ map, float *__restrict__ dense) {
+    __shared__ __align__(16) float s_dense[kRoutingWarps][kMaxE];
+    __shared__ __align__(16) uint8_t s_map[kRoutingWarps][kMaxE];
+    pdl_wait();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float *sd = s_dense[warp];
+    uint8_t *sm = s_map[warp];
+    const int n16 = E / 16;   // 16-byte chunks of a map row (a dense row has 4 * n16)
+    const uint4 z4 = make_uint4(0, 0, 0, 0);
+    for (int t = blockIdx.x * kRoutingWarps + warp; t < T; t += gridDim.x * kRoutingWarps) {
+        const int my_id = lane < K ? ids[(size_t)t * K + lane] : -1;
+        const float my_p = (lane < K && probs) ? probs[(size_t)t * K + lane] : 0.0f;
+        const bool valid = my_id >= 0 && my_id < E;
+        for (int c = lane; c < n16; c += 32) reinterpret_cast<uint4 *>(sm)[c] = z4;
+        if (dense)
+            for (int c = lane; c < 4 * n16; c += 32) reinterpret_cast<uint4 *>(sd)[c] = z4;
+        bool first = valid;
+        float acc = 0.0f;
+        for (int k = 0; k < K; ++k) {
+            const int id = __shfl_sync(kFullMask, my_id, k);
+            const float p = __shfl_sync(kFullMask, my_p, k);
+            if (valid && id == my_id) {
+                if (k < lane) first = false;
+                acc = __fadd_rn(acc, p);
+            }
+        }
+        __syncwarp();   // the row is zero before any expert is set
+        if (first) {
+            sm[my_id] = 1;
+            if (dense) sd[my_id] = acc;
+        }
+        __syncwarp();
+        uint8_t *mrow = map + (size_t)t * E;
+        for (int c = lane; c < n16; c += 32)
+            reinterpret_cast<uint4 *>(mrow)[c] = reinterpret_cast<const uint4 *>(sm)[c];
+        if (dense) {
+            float *drow = dense + (size_t)t * E;
+            for (int c = lane; c < 4 * n16; c += 32)
+                reinterpret_cast<uint4 *>(drow)[c] = reinterpret_cast<const uint4 *>(sd)[c];
+        }
+        __syncwarp();   // every lane has read the row before the next token clears it
+    }
+}
+
 inline int routing_grid(int T) {
     int grid = (T + kRoutingWarps - 1) / kRoutingWarps;
     const int cap = 152 * 8;
@@ -200,6 +252,9 @@ extern "C" int ep_indices_to_multihot(const int32_t *topk_ids, const float *topk
         (routing_map && !aligned16(routing_map)) || (dense_probs && !aligned16(dense_probs)))
         return EP_ERR_INVALID_ARG;
     if (T == 0) return EP_OK;
+    if (E % 16 == 0)   // every map row starts on a 16-byte boundary
+        return launch_pdl(ep_indices_to_multihot_wide_kernel, dim3(routing_grid(T)), dim3(kRoutingThreads),
+                          0, as_stream(stream), topk_ids, topk_probs, T, K, E, routing_map, dense_probs);
     return launch_pdl(ep_indices_to_multihot_kernel, dim3(routing_grid(T)), dim3(kRoutingThreads), 0,
                       as_stream(stream), topk_ids, topk_probs, T, K, E, routing_map, dense_probs);
 }
