@@ -485,6 +485,9 @@ def run_ours(args, cfg):
             stream=stream),
         f"dispatch_nvfp4 (pad {PAD})": lambda: ep.dispatch_nvfp4(x, Lp, out=(p_fp4, p_sc, p_inv, p_so),
                                                                  stream=stream),
+        f"layout+dispatch_nvfp4 (pad {PAD}, fused call)": lambda: ep.dispatch_layout_padded_nvfp4(
+            ids, x, E, P, C, bool(S), PAD, None, out_layout=Lp, out=(p_fp4, p_sc, p_inv, p_so),
+            stream=stream),
     }
     extra = {}
     for name, fn in extra_fns.items():
@@ -569,6 +572,7 @@ def run_ours(args, cfg):
     pb = padded_bytes(cfg, R_pad)
     ab[f"layout (pad {PAD})"] = pb["layout"]
     ab[f"dispatch_nvfp4 (pad {PAD})"] = pb["dispatch_nvfp4"]
+    ab[f"layout+dispatch_nvfp4 (pad {PAD}, fused call)"] = pb["layout"] + pb["dispatch_nvfp4"]
     peak, peak_kind = load_peaks()
     achieved = ab["combine"] / comb_s / 1e9
     traffic = recorded_traffic("combine_dsv3")
@@ -618,7 +622,8 @@ def run_ours(args, cfg):
                          f"from the routing as a dense map (map -> ids, then the layout), "
                          f"indices_to_multihot, and the layout and NVFP4 dispatch with groups padded to "
                          f"{PAD} rows ({R_pad} rows, {R_pad - R} of them padding, written as an "
-                         f"all-zero token)"),
+                         f"all-zero token), as two calls and as one ep_dispatch_layout_padded_nvfp4 "
+                         f"call"),
         "static_routing_step": static,
         "graph_replay": graphs,
         "configs_sweep": sweep,
@@ -892,8 +897,9 @@ def graph_replay(ep, dev, stream, flush_l2, n_steps: int) -> list:
 
 def static_routing_step(ep, dev, stream, flush_l2, n_steps: int) -> dict:
     """Layout + NVFP4 dispatch + combine on the forced-balanced static routing workload, with its
-    persisted row count passed as the static row capacity and groups padded to 128 rows; L2
-    flushed before each step, events around it."""
+    persisted row count passed as the static row capacity and groups padded to 128 rows: the
+    padded layout + NVFP4 call then combine, and for comparison the layout and the dispatch as
+    two calls.  L2 flushed before each step, events around it."""
     import torch
     cfg = W.CONFIGS["dsv3_static"]
     T, H, E, K, S, P, C = cfg.T, cfg.H, cfg.E, cfg.K, cfg.S, cfg.P, cfg.capacity
@@ -911,7 +917,12 @@ def static_routing_step(ep, dev, stream, flush_l2, n_steps: int) -> dict:
     so = torch.empty(E + S + 1, dtype=torch.int32, device=dev)
     out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
 
-    def step():
+    def step():   # the padded layout and the NVFP4 dispatch in one call, then combine
+        ep.dispatch_layout_padded_nvfp4(ids, x, E, P, C, bool(S), cfg.pad_multiple, cfg.num_permuted_tokens,
+                                        out_layout=Ls, out=(fp4, sc, inv, so), stream=stream)
+        ep.combine(y, probs, Ls, out=out, stream=stream)
+
+    def step_two_calls():
         ep.dispatch_layout_routed(E, topk_ids=ids, n_parts=P, capacity=C, fused_shared=bool(S),
                                   pad_multiple=cfg.pad_multiple,
                                   num_permuted_tokens=cfg.num_permuted_tokens, out=Ls, stream=stream)
@@ -923,18 +934,23 @@ def static_routing_step(ep, dev, stream, flush_l2, n_steps: int) -> dict:
     if ep.read_status(Ls) != 0:
         raise RuntimeError("static routing layout reported an error")
     R = int(Ls.row_offsets[Ls.G].item())
-    for _ in range(3):
-        flush_l2()
-        step()
-    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for _ in range(n_steps)]
-    for a, b in pairs:
-        flush_l2()
-        a.record(stream)
-        step()
-        b.record(stream)
-    torch.cuda.synchronize(dev)
-    sec = float(np.mean([a.elapsed_time(b) for a, b in pairs])) * 1e-3
+
+    def timed(fn):
+        for _ in range(3):
+            flush_l2()
+            fn()
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(n_steps)]
+        for a, b in pairs:
+            flush_l2()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        return float(np.mean([a.elapsed_time(b) for a, b in pairs])) * 1e-3
+
+    sec = timed(step)
+    sec_two = timed(step_two_calls)
     ab = algorithmic_bytes(cfg, R)
     nbytes = ab["layout"] + ab["dispatch_nvfp4"] + ab["combine"]
     return {"workload": f"{cfg.name}: T={T}, hidden={H}, {E} experts, top-{K}, shared expert, "
@@ -942,7 +958,9 @@ def static_routing_step(ep, dev, stream, flush_l2, n_steps: int) -> dict:
                         f"static row capacity {cfg.num_permuted_tokens}",
             "us_per_step": sec * 1e6, "tokens/s": T / sec, "rows": R, "algorithmic_bytes": nbytes,
             "GB/s": nbytes / sec / 1e9, "steps": n_steps,
-            "calls": "ep_dispatch_layout_routed + ep_dispatch_nvfp4 (+ padding fill) + ep_combine"}
+            "calls": "ep_dispatch_layout_padded_nvfp4 (+ padding fill) + ep_combine",
+            "us_per_step_two_calls": sec_two * 1e6,
+            "two_calls": "ep_dispatch_layout_routed + ep_dispatch_nvfp4 (+ padding fill) + ep_combine"}
 
 
 ONLY_OPS = ("layout", "layout_noalloc", "dispatch_layout_nvfp4", "dispatch_nvfp4", "dispatch_bf16",

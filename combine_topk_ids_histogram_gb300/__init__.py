@@ -7,7 +7,7 @@ the built library raises.
 
 Entry points (same names as the C ABI, without the ``ep_`` prefix):
 ``dispatch_layout``, ``dispatch_layout_routed``, ``dispatch_layout_noalloc``, ``dispatch_nvfp4``,
-``dispatch_layout_nvfp4``, ``dispatch_bf16``, ``dispatch_fp8``, ``combine``, ``combine_bwd``,
+``dispatch_layout_nvfp4``, ``dispatch_layout_padded_nvfp4``, ``dispatch_bf16``, ``dispatch_fp8``, ``combine``, ``combine_bwd``,
 ``dispatch_bwd``, ``routing_map_to_topk``, ``indices_to_multihot``, ``rows_max``,
 ``read_status``, ``cvt_e2m1``, ``cvt_e4m3``.
 """
@@ -79,6 +79,8 @@ SIGNATURES = {
     "ep_dispatch_layout_noalloc": (_I, [_P, _I, _I, _I, _I, _I, _I, _LP, _P]),
     "ep_dispatch_nvfp4": (_I, [_P, _I, _LP, _P, _P, _P, _P, _P]),
     "ep_dispatch_layout_nvfp4": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _I, _LP, _P, _P, _P, _P, _P]),
+    "ep_dispatch_layout_padded_nvfp4": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _LP, _P, _P, _P,
+                                             _P, _P]),
     "ep_dispatch_bf16": (_I, [_P, _I, _LP, _P, _P]),
     "ep_combine": (_I, [_P, _P, _I, _LP, _P, _P]),
     "ep_combine_bwd": (_I, [_P, _P, _P, _I, _LP, _P, _P, _P]),
@@ -442,6 +444,56 @@ def dispatch_layout_nvfp4(topk_ids: torch.Tensor, x: torch.Tensor, n_experts: in
                                        S, _bits(x) if T > 0 else None, H, L.ref, _ptr(fp4), _ptr(sc),
                                        _bits(inv), _ptr(so), _stream(stream))
     _check(rc, "ep_dispatch_layout_nvfp4")
+    return L, out
+
+
+def _nvfp4_out(L: Layout, H: int, out, dev):
+    if out is None:
+        out = (torch.empty(max(L.R_max, 1), H // 2, dtype=torch.uint8, device=dev),
+               torch.empty(max(L.R_max, 1), H // 16, dtype=torch.uint8, device=dev),
+               torch.empty(max(L.R_max, 1), dtype=torch.bfloat16, device=dev),
+               torch.empty(L.G + 1, dtype=torch.int32, device=dev))
+    fp4, sc, inv, so = out
+    _need(fp4, L.R_max, H // 2, (torch.uint8,), "out_fp4")
+    _need(sc, L.R_max, H // 16, (torch.uint8,), "out_scales")
+    _need(inv, L.R_max, None, _BF16, "out_rowwise_inv_scale")
+    _need(so, L.G + 1, None, (torch.int32,), "scales_offsets")
+    return out
+
+
+def dispatch_layout_padded_nvfp4(topk_ids: torch.Tensor, x: torch.Tensor, n_experts: int,
+                                 n_parts: int = 1, capacity: int | None = None,
+                                 fused_shared: bool = False, pad_multiple: int = 1,
+                                 num_permuted_tokens: int | None = None,
+                                 out_layout: Layout | None = None, out=None, stream=None):
+    """ep_dispatch_layout_padded_nvfp4: the layout of ``dispatch_layout_routed`` from compact ids
+    (groups padded to ``pad_multiple`` rows, optional static row capacity) and the NVFP4
+    dispatch in one call; padding rows get the dispatch of an all-zero token.  Returns
+    (Layout, (fp4, scales, inv, scales_offsets))."""
+    if topk_ids.dtype != torch.int32 or topk_ids.dim() != 2:
+        raise TypeError("topk_ids must be an int32 [T, K] tensor")
+    T, K = topk_ids.shape
+    Tx, H = x.shape
+    if Tx != T:
+        raise ValueError("x and topk_ids disagree on the number of tokens")
+    S = int(bool(fused_shared))
+    key = (T, K, n_experts, n_parts, S, int(pad_multiple), int(num_permuted_tokens or 0))
+    L = out_layout
+    if L is not None and L.shape_key() != key:
+        raise ValueError(f"layout buffers were allocated for other sizes {L.shape_key()}")
+    if L is None:
+        L = Layout(T, K, n_experts, n_parts, fused_shared, topk_ids.device, pad_multiple,
+                   num_permuted_tokens)
+    _need(x, None, H, _BF16, "input_tokens", exact_rows=T)
+    out = _nvfp4_out(L, H, out, x.device)
+    fp4, sc, inv, so = out
+    cap = T if capacity is None else int(capacity)
+    L.capacity = cap
+    rc = _lib.ep_dispatch_layout_padded_nvfp4(
+        _ptr(topk_ids) if T > 0 else None, T, K, n_experts, n_parts, cap, S, int(pad_multiple),
+        int(num_permuted_tokens or 0), _bits(x) if T > 0 else None, H, L.ref, _ptr(fp4), _ptr(sc),
+        _bits(inv), _ptr(so), _stream(stream))
+    _check(rc, "ep_dispatch_layout_padded_nvfp4")
     return L, out
 
 

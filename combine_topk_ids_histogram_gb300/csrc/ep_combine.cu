@@ -43,7 +43,7 @@ ep_combine_kernel(const uint16_t *__restrict__ y, const float *__restrict__ prob
     __shared__ int s_rows[2][KMAX + 1];
     __shared__ float s_w[2][KMAX + 1];
     pdl_begin();
-    if (load_status(status)) return;
+    if (cta_status(status)) return;
     const int tid = threadIdx.x;
     const int shared_base = S ? row_offsets[E] : 0;
 
@@ -134,7 +134,7 @@ ep_combine_bwd_kernel(const uint16_t *__restrict__ g, const uint16_t *__restrict
     __shared__ float s_p[KMAX];
     __shared__ float s_red[kCombineThreads / 32][KMAX];
     pdl_wait();
-    if (load_status(status)) return;
+    if (cta_status(status)) return;
     if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: zero gradient rows
         fill_group_padding(blockIdx.x / fparts, blockIdx.x % fparts, fparts, pad, R_max, row_offsets,
                            src_info, status, PadFill{grad_y, 2 * H, 0u}, PadFill{nullptr, 0, 0u},

@@ -62,6 +62,16 @@ __device__ __forceinline__ int load_status(const int32_t *status) {
 #endif
 constexpr bool kBoundsCheck = EP_BOUNDS_CHECK != 0;
 
+// The status word as one value for the whole CTA; every thread of the CTA must call it.  Only
+// the layout writes the word, and it completes before any kernel that reads it starts, so in
+// the default build every thread reads the same value.  In the bounds-checked build another CTA
+// of the running kernel may set EP_STATUS_BOUNDS meanwhile, so the CTA agrees on one reading
+// (one barrier) before it acts on it.
+__device__ __forceinline__ int cta_status(const int32_t *status) {
+    if (kBoundsCheck) return __syncthreads_or(load_status(status));
+    return load_status(status);
+}
+
 // Records a failed check in the status word (checked build only).
 __device__ __forceinline__ void bounds_fail(const int32_t *status) {
     if (kBoundsCheck) atomicOr(const_cast<int32_t *>(status), EP_STATUS_BOUNDS);

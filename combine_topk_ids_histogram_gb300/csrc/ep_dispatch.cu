@@ -63,7 +63,7 @@ ep_dispatch_nvfp4_kernel(const uint16_t *__restrict__ x, int T, int H, int K, in
     //             while the layout still runs, and the layout's outputs are read after the wait.
     if (!early) pdl_wait();
     if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: a group's padding rows
-        if (!load_status(status))
+        if (!cta_status(status))
             fill_group_padding_call(blockIdx.x / fparts, blockIdx.x % fparts, fparts, pad, R_max,
                                     row_offsets, src_info, status, f0, f1, f2);
         return;
@@ -107,7 +107,7 @@ ep_dispatch_nvfp4_kernel(const uint16_t *__restrict__ x, int T, int H, int K, in
             else if (tid == K && S) my_row = row_offsets[E] + t;
         }
     }
-    if (load_status(status)) return;
+    if (cta_status(status)) return;
     if (t == 0)
         for (int gi = tid; gi <= G; gi += blockDim.x) scales_offsets[gi] = row_offsets[gi];
     if (t >= T) return;
@@ -157,7 +157,7 @@ ep_dispatch_bf16_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int
                         const int32_t *__restrict__ status, uint16_t *__restrict__ out, PadFill f0) {
     __shared__ int s_rows[kMaxRowsPerToken];
     pdl_wait();
-    if (load_status(status)) return;
+    if (cta_status(status)) return;
     if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: a group's padding rows
         fill_group_padding_call(blockIdx.x / fparts, blockIdx.x % fparts, fparts, pad, R_max,
                                 row_offsets, src_info, status, f0, PadFill{nullptr, 0, 0u},
@@ -215,7 +215,7 @@ ep_dispatch_fp8_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int 
     __shared__ int s_rows[kMaxRowsPerToken];
     pdl_wait();
     if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: a group's padding rows
-        if (!load_status(status))
+        if (!cta_status(status))
             fill_group_padding_call(blockIdx.x / fparts, blockIdx.x % fparts, fparts, pad, R_max,
                                     row_offsets, src_info, status, f0, f1, PadFill{nullptr, 0, 0u});
         return;
@@ -235,7 +235,7 @@ ep_dispatch_fp8_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int 
     int my_row = -1;
     if (tid < K) my_row = row_of[(size_t)t * K + tid];
     else if (tid == K && S) my_row = row_offsets[E] + t;
-    if (load_status(status)) return;
+    if (cta_status(status)) return;
     if (tid < K + S) s_rows[tid] = my_row;
     float m = absmax_value(max_u16x2(max_u16x2(absmax_bits(v[0]), absmax_bits(v[1])),
                                      max_u16x2(absmax_bits(v[2]), absmax_bits(v[3]))));
@@ -301,7 +301,9 @@ ep_dispatch_fp8_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int 
 // With `write_meta` set the layout kernel left src_info and expert_ids to this kernel: each lane
 // that sends a row also writes that row's (token, slot) and expert, so the layout's critical
 // path carries only row_of.  The metadata is written even when the status word stops the
-// payload, as the layout would have written it.
+// payload, as the layout would have written it.  For a padded layout (pad > 1) the CTAs also
+// write each group's padding rows as the dispatch of an all-zero token once their own rows are
+// out, fparts CTAs to a group.
 // ---------------------------------------------------------------------------------------
 constexpr int kStageSlots = 8;
 constexpr int kStageMaxThreads = 256;
@@ -317,7 +319,8 @@ __device__ __forceinline__ void write_row_meta(int r, int t, int k, int K, int E
 
 __global__ void __launch_bounds__(kStageMaxThreads, 4)
 ep_dispatch_nvfp4_staged_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int E, int S, int G,
-                                int R_max, int early, int write_meta, const int32_t *__restrict__ ids,
+                                int R_max, int early, int write_meta, int pad, int fparts,
+                                const int32_t *__restrict__ ids,
                                 const int32_t *__restrict__ row_of,
                                 const int32_t *__restrict__ row_offsets,
                                 const int32_t *__restrict__ status, uint8_t *__restrict__ out_fp4,
@@ -404,7 +407,7 @@ ep_dispatch_nvfp4_staged_kernel(const uint16_t *__restrict__ x, int T, int H, in
         }
         const int shared_base = S ? row_offsets[E] : 0;
         const int nrows = K + S;
-        if (load_status(status)) {         // constant per call: no copy was issued before
+        if (cta_status(status)) {         // constant per call: no copy was issued before
             if (write_meta)                // no payload, but every row's metadata
                 for (int t = tb + warp; t < te; t += nwarps)
                     for (int k = lane; k < nrows; k += 32) {
@@ -433,6 +436,13 @@ ep_dispatch_nvfp4_staged_kernel(const uint16_t *__restrict__ x, int T, int H, in
         __syncthreads();
     }
     if (!waited) pdl_begin();       // a CTA without tokens still orders itself after the layout
+    if (pad > 1 && !cta_status(status)) {   // padding rows: codes 0, scales 0, inverse bf16(1)
+        const PadFill f0{out_fp4, (int)code_bytes, 0u}, f1{out_scales, (int)scale_bytes, 0u},
+            f2{out_inv, 2, 0x3F803F80u};
+        for (int q = blockIdx.x; q < G * fparts; q += gridDim.x)
+            fill_group_padding(q / fparts, q % fparts, fparts, pad, R_max, row_offsets, src_info, status,
+                               f0, f1, f2);
+    }
     bulk_wait_all();                // every copy of this thread has landed
 }
 
@@ -465,7 +475,8 @@ inline int staged_grid(int T, int K, int H, int busy_sms) {
 }
 
 // The staged dispatch on `grid` CTAs (from staged_grid); with write_meta it also writes the
-// layout's src_info and expert_ids (the layout kernel before it left them out).
+// layout's src_info and expert_ids (the layout kernel before it left them out), and for a padded
+// layout it writes the padding rows.
 inline int launch_nvfp4_staged(int grid, const uint16_t *x, int H, const int32_t *ids,
                                const ep_layout_t *L, uint8_t *out_fp4, uint8_t *out_scales,
                                uint16_t *out_inv, int32_t *scales_offsets, int early, int write_meta,
@@ -474,8 +485,10 @@ inline int launch_nvfp4_staged(int grid, const uint16_t *x, int H, const int32_t
     const size_t smem = (size_t)kStageSlots * ((size_t)H / 2 + H / 16) + 2 * kStageSlots;
     const int G = L->E + L->fused_shared;
     const int R_max = layout_rows(L);
+    const int pad = layout_padded(L) ? L->pad_multiple : 1;
     return launch_pdl(ep_dispatch_nvfp4_staged_kernel, dim3(grid), dim3(threads), smem, st, x, L->T, H,
-                      L->K, L->E, L->fused_shared, G, R_max, early, write_meta, ids,
+                      L->K, L->E, L->fused_shared, G, R_max, early, write_meta, pad,
+                      fill_parts(L, threads), ids,
                       (const int32_t *)L->row_of, (const int32_t *)L->row_offsets,
                       (const int32_t *)L->status, out_fp4, out_scales, out_inv, scales_offsets,
                       L->src_info, L->expert_ids);
@@ -593,6 +606,38 @@ extern "C" int ep_dispatch_layout_nvfp4(const int32_t *topk_ids, int T, int K, i
                                    meta_in_dispatch && layout_sms > 0, st);
     return launch_nvfp4(input_tokens, H, L, out_fp4, out_scales, out_rowwise_inv_scale,
                         scales_offsets, 1, st);
+}
+
+extern "C" int ep_dispatch_layout_padded_nvfp4(const int32_t *topk_ids, int T, int K, int n_experts,
+                                               int n_parts, int capacity, int fused_shared,
+                                               int pad_multiple, int num_permuted_tokens,
+                                               const uint16_t *input_tokens, int hidden_size,
+                                               ep_layout_t *L, uint8_t *out_fp4, uint8_t *out_scales,
+                                               uint16_t *out_rowwise_inv_scale, int32_t *scales_offsets,
+                                               void *stream) {
+    const int H = hidden_size;
+    if (!hidden_ok(H) || H / 16 > 1024) return EP_ERR_INVALID_ARG;
+    if ((T > 0 && (!input_tokens || !out_fp4 || !out_scales || !out_rowwise_inv_scale)) ||
+        !scales_offsets)
+        return EP_ERR_INVALID_ARG;
+    const void *ptrs[] = {input_tokens, out_fp4, out_scales, out_rowwise_inv_scale, scales_offsets};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return EP_ERR_INVALID_ARG;
+    cudaStream_t st = as_stream(stream);
+    // As in ep_dispatch_layout_nvfp4 the staged dispatch quantises while the layout runs; the
+    // layout writes every row's metadata (the padding rows' too), and the dispatch writes the
+    // padding rows' payload.  Without the staged kernel, the per-token kernel runs after the
+    // layout with its leading padding CTAs, as ep_dispatch_nvfp4 would.
+    const int grid = staged_grid(T, K, H, layout_cluster_plan(T, K, n_experts, n_parts));
+    int layout_sms = 0;
+    int rc = launch_layout(topk_ids, T, K, n_experts, n_parts, capacity, fused_shared, pad_multiple,
+                           num_permuted_tokens, L, st, &layout_sms, 1);
+    if (rc != EP_OK) return rc;
+    if (grid > 0)
+        return launch_nvfp4_staged(grid, input_tokens, H, topk_ids, L, out_fp4, out_scales,
+                                   out_rowwise_inv_scale, scales_offsets, 1, 0, st);
+    return launch_nvfp4(input_tokens, H, L, out_fp4, out_scales, out_rowwise_inv_scale,
+                        scales_offsets, 0, st);
 }
 
 extern "C" int ep_dispatch_bf16(const uint16_t *input_tokens, int hidden_size, const ep_layout_t *L,

@@ -264,6 +264,31 @@ int ep_dispatch_layout_nvfp4(const int32_t *topk_ids, int T, int K, int n_expert
                              int32_t *scales_offsets, void *stream);
 
 /*
+ * ep_dispatch_layout_padded_nvfp4 -- ep_dispatch_layout_routed from compact ids (routing_map
+ * NULL), with groups padded to pad_multiple rows and an optional static row capacity, followed
+ * by ep_dispatch_nvfp4, in one call.
+ * Defined by: token_dispatcher, TokenDispatcherConfig.moe_router_expert_pad_multiple and
+ * moe_benchmark_static_routing (padded groups, a persisted row count); fused_a2a,
+ * HybridEPDispatch.forward (pad_multiple, num_permuted_tokens; fuse_permute); Mojo EP dispatch,
+ * execute (NVFP4 quantisation in the dispatch).
+ *
+ * Arguments are those of ep_dispatch_layout_routed (without the routing map and its outputs)
+ * followed by those of ep_dispatch_nvfp4, and the results are identical to calling the two in
+ * sequence: every padding row receives the dispatch of an all-zero token (codes 0, block scales
+ * 0, inverse scale bf16(1)), rows at or past row_offsets[G] are untouched, and nothing but the
+ * layout is written when the status word is set.  As in ep_dispatch_layout_nvfp4, the
+ * quantisation of input_tokens overlaps the layout.  The buffers hold R_max rows, as
+ * ep_rows_max(T, K, E, S, pad_multiple, num_permuted_tokens) gives.  Errors are those of the
+ * two calls.
+ */
+int ep_dispatch_layout_padded_nvfp4(const int32_t *topk_ids, int T, int K, int n_experts,
+                                    int n_parts, int capacity, int fused_shared, int pad_multiple,
+                                    int num_permuted_tokens, const uint16_t *input_tokens,
+                                    int hidden_size, ep_layout_t *L, uint8_t *out_fp4,
+                                    uint8_t *out_scales, uint16_t *out_rowwise_inv_scale,
+                                    int32_t *scales_offsets, void *stream);
+
+/*
  * ep_dispatch_bf16 -- scatter every token into its rows unchanged.
  * Defined by: fused_a2a, HybridEPDispatch.forward / hybrid_ep_dispatch (dispatched hidden
  * states [dispatched_tokens, hidden] grouped by expert).

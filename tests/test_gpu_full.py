@@ -49,6 +49,13 @@ def ep():
     return ep
 
 
+def new_layout_padded(ep, T, K, E, P, S, pad, cap):
+    L = ep.Layout(T, K, E, P, bool(S), pad_multiple=pad, num_permuted_tokens=cap)
+    L.expert_ids.fill_(-7)
+    L.src_info.fill_(-7)
+    return L
+
+
 def filled(shape, bits, dtype):
     """A device buffer holding the oracle's fill pattern (16-bit fills as int16 bit patterns)."""
     if dtype == torch.uint8:
@@ -226,8 +233,21 @@ def test_full_size_padded(ep, name, pad, cap):
     assert np.array_equal(L.expert_ids.cpu().numpy()[:ref.R], ref.expert_ids[:ref.R])
     assert np.array_equal(L.src_info.cpu().numpy()[:ref.R], ref.src_info[:ref.R])
     bufs = nvfp4_buffers(ref.R_max, H, E, S)
-    ep.dispatch_nvfp4(dev_bf16(x), L, out=bufs)
-    check_nvfp4_full(bufs, oracle.dispatch_nvfp4(x, ref, fill=FILL8), f"{name} padded NVFP4")
+    xd = dev_bf16(x)
+    ep.dispatch_nvfp4(xd, L, out=bufs)
+    ref_rows = oracle.dispatch_nvfp4(x, ref, fill=FILL8)
+    check_nvfp4_full(bufs, ref_rows, f"{name} padded NVFP4")
+    # the fused padded layout + NVFP4 call the static-routing benchmark step makes
+    Lf = new_layout_padded(ep, T, K, E, P, S, pad, cap)
+    fbufs = nvfp4_buffers(ref.R_max, H, E, S)
+    ep.dispatch_layout_padded_nvfp4(dev(ids), xd, E, P, C, bool(S), pad, cap, out_layout=Lf, out=fbufs)
+    assert ep.read_status(Lf) == 0
+    assert np.array_equal(Lf.row_offsets.cpu().numpy(), ref.row_offsets)
+    assert np.array_equal(Lf.row_of.cpu().numpy(), ref.row_of)
+    assert np.array_equal(Lf.expert_ids.cpu().numpy()[:ref.R], ref.expert_ids[:ref.R])
+    assert np.array_equal(Lf.src_info.cpu().numpy()[:ref.R], ref.src_info[:ref.R])
+    check_nvfp4_full(fbufs, ref_rows, f"{name} fused padded layout + NVFP4")
+    del ref_rows, fbufs
     y_host = np.resize(W.make_expert_out(cfg), (ref.R_max, H)).astype(np.uint16)
     out = ep.combine(dev_bf16(y_host), dev(probs), L)
     check_combine_full(out, y_host, probs, ref, f"{name} padded combine")

@@ -84,6 +84,21 @@ def test_random_case(ep, seed):
     assert np.array_equal(out[1].cpu().numpy(), rsc)
     assert np.array_equal(host_bf16(out[2]), rinv)
 
+    # the fused padded layout + NVFP4 call: the same layout and rows
+    Lf = ep.Layout(T, K, E, P, bool(S), pad_multiple=pad, num_permuted_tokens=cap)
+    outf = tuple(torch.full_like(o, f) for o, f in zip(out, (0xA5, 0xA5, 0, -7)))
+    outf[2].view(torch.int16).fill_(-23131)
+    ep.dispatch_layout_padded_nvfp4(ids_d, xd, E, P, C, bool(S), pad, cap, out_layout=Lf, out=outf)
+    assert ep.read_status(Lf) == ref.status
+    assert np.array_equal(Lf.row_offsets.cpu().numpy(), ref.row_offsets)
+    assert np.array_equal(Lf.row_of.cpu().numpy(), ref.row_of)
+    assert np.array_equal(Lf.expert_ids.cpu().numpy()[:n], ref.expert_ids[:n])
+    assert np.array_equal(Lf.src_info.cpu().numpy()[:n], ref.src_info[:n])
+    assert np.array_equal(outf[0].cpu().numpy(), rfp4)
+    assert np.array_equal(outf[1].cpu().numpy(), rsc)
+    assert np.array_equal(host_bf16(outf[2]), rinv)
+    assert np.array_equal(outf[3].cpu().numpy(), rso)
+
     rows = torch.full((Rm, H), -23131, dtype=torch.int16, device="cuda").view(torch.bfloat16)
     ep.dispatch_bf16(xd, L, out=rows)
     assert np.array_equal(host_bf16(rows), oracle.dispatch_bf16(x, ref, fill=0xA5A5))

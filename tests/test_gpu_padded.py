@@ -1,8 +1,9 @@
 """GPU vs oracle parity of padded layouts, static row capacities and the padding rows every
 dispatch writes (token_dispatcher page, TokenDispatcherConfig.moe_router_expert_pad_multiple
 and moe_benchmark_static_routing; fused_a2a page, HybridEPDispatch.forward pad_multiple and
-num_permuted_tokens).  Layout, codes, scales and bf16 rows are bit-exact; combine and the
-backward passes are within the tolerances of gpu_helpers."""
+num_permuted_tokens), through the separate calls and the fused padded layout + NVFP4 call.
+Layout, codes, scales and bf16 rows are bit-exact; combine and the backward passes are within
+the tolerances of gpu_helpers."""
 import numpy as np
 import pytest
 import torch
@@ -46,6 +47,27 @@ def check_padded_layout(ep, L, ref):
     assert (ei[n:ref.R_max] == CANARY32).all() and (si[n:ref.R_max] == CANARY32).all()
 
 
+def check_fused_padded(ep, cfg, ids, xd, pad, cap, ref, ref_rows):
+    """ep_dispatch_layout_padded_nvfp4 gives the layout and NVFP4 rows (padding rows included)
+    of the two separate calls."""
+    L = ep.Layout(cfg.T, cfg.K, cfg.E, cfg.P, bool(cfg.S), pad_multiple=pad, num_permuted_tokens=cap)
+    L.expert_ids.fill_(CANARY32)
+    L.src_info.fill_(CANARY32)
+    Rm, H = ref.R_max, xd.shape[1]
+    out = (torch.full((Rm, H // 2), 0xA5, dtype=torch.uint8, device="cuda"),
+           torch.full((Rm, H // 16), 0xA5, dtype=torch.uint8, device="cuda"),
+           torch.full((Rm,), -23131, dtype=torch.int16, device="cuda").view(torch.bfloat16),
+           torch.full((cfg.E + cfg.S + 1,), -7, dtype=torch.int32, device="cuda"))
+    ep.dispatch_layout_padded_nvfp4(dev(ids), xd, cfg.E, cfg.P, cfg.capacity, bool(cfg.S), pad, cap,
+                                    out_layout=L, out=out)
+    check_padded_layout(ep, L, ref)
+    rfp4, rsc, rinv, rso = ref_rows
+    assert np.array_equal(out[0].cpu().numpy(), rfp4), "fused call: NVFP4 codes"
+    assert np.array_equal(out[1].cpu().numpy(), rsc), "fused call: E4M3 scales"
+    assert np.array_equal(host_bf16(out[2]), rinv), "fused call: inverse scales"
+    assert np.array_equal(out[3].cpu().numpy(), rso), "fused call: scales_offsets"
+
+
 def run_all(ep, cfg, pad, cap, x=None, ids=None, probs=None, y=None):
     inp = W.make_inputs(cfg) if ids is None else None
     ids = inp["topk_ids"] if ids is None else ids
@@ -70,6 +92,7 @@ def run_all(ep, cfg, pad, cap, x=None, ids=None, probs=None, y=None):
     assert np.array_equal(host_bf16(out[2]), rinv), "inverse scales"
     if not ref.status:
         assert np.array_equal(out[3].cpu().numpy(), rso)
+    check_fused_padded(ep, cfg, ids, xd, pad, cap, ref, (rfp4, rsc, rinv, rso))
 
     rows = torch.full((Rm, H), -23131, dtype=torch.int16, device="cuda").view(torch.bfloat16)
     ep.dispatch_bf16(xd, L, out=rows)
