@@ -301,9 +301,10 @@ ep_dispatch_fp8_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int 
 // With `write_meta` set the layout kernel left src_info and expert_ids to this kernel: each lane
 // that sends a row also writes that row's (token, slot) and expert, so the layout's critical
 // path carries only row_of.  The metadata is written even when the status word stops the
-// payload, as the layout would have written it.  For a padded layout (pad > 1) the CTAs also
-// write each group's padding rows as the dispatch of an all-zero token once their own rows are
-// out, fparts CTAs to a group.
+// payload, as the layout would have written it.  For a padded layout (pad > 1), CTAs after the
+// first tok_ctas write each group's padding rows as the dispatch of an all-zero token, fparts
+// of them to a group.  The block scheduler places them once slots free up: on the SMs the
+// layout leaves when it ends, and where token CTAs have finished.
 // ---------------------------------------------------------------------------------------
 constexpr int kStageSlots = 8;
 constexpr int kStageMaxThreads = 256;
@@ -320,7 +321,7 @@ __device__ __forceinline__ void write_row_meta(int r, int t, int k, int K, int E
 __global__ void __launch_bounds__(kStageMaxThreads, 4)
 ep_dispatch_nvfp4_staged_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int E, int S, int G,
                                 int R_max, int early, int write_meta, int pad, int fparts,
-                                const int32_t *__restrict__ ids,
+                                int tok_ctas, const int32_t *__restrict__ ids,
                                 const int32_t *__restrict__ row_of,
                                 const int32_t *__restrict__ row_offsets,
                                 const int32_t *__restrict__ status, uint8_t *__restrict__ out_fp4,
@@ -330,6 +331,16 @@ ep_dispatch_nvfp4_staged_kernel(const uint16_t *__restrict__ x, int T, int H, in
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ __align__(16) float s_red[2][kStageMaxThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if ((int)blockIdx.x >= tok_ctas) {   // trailing CTAs of a padded layout: padding rows
+        pdl_wait();
+        if (!cta_status(status)) {      // codes 0, block scales 0, inverse scale bf16(1)
+            const int q = blockIdx.x - tok_ctas;
+            const PadFill f0{out_fp4, H / 2, 0u}, f1{out_scales, H / 16, 0u}, f2{out_inv, 2, 0x3F803F80u};
+            fill_group_padding(q / fparts, q % fparts, fparts, pad, R_max, row_offsets, src_info, status,
+                               f0, f1, f2);
+        }
+        return;
+    }
     const int nwarps = blockDim.x >> 5;
     // The slots of absent warps (which no warp writes) hold 0, so every step reads all eight
     // with two 16-byte loads; the first step's barrier orders these stores before the reads.
@@ -343,8 +354,8 @@ ep_dispatch_nvfp4_staged_kernel(const uint16_t *__restrict__ x, int T, int H, in
     uint16_t *s_inv = reinterpret_cast<uint16_t *>(smem_raw + (size_t)kStageSlots * slot_bytes);
     // Token ranges of ceil(T / grid) or floor(T / grid) tokens: every SM gets the same number
     // of CTAs and each CTA within one token of the same work.
-    const int tb = (int)((long long)blockIdx.x * T / gridDim.x);
-    const int te = (int)((long long)(blockIdx.x + 1) * T / gridDim.x);
+    const int tb = (int)((long long)blockIdx.x * T / tok_ctas);
+    const int te = (int)((long long)(blockIdx.x + 1) * T / tok_ctas);
     bool waited = false;
     if (!early) {
         pdl_begin();
@@ -436,13 +447,6 @@ ep_dispatch_nvfp4_staged_kernel(const uint16_t *__restrict__ x, int T, int H, in
         __syncthreads();
     }
     if (!waited) pdl_begin();       // a CTA without tokens still orders itself after the layout
-    if (pad > 1 && !cta_status(status)) {   // padding rows: codes 0, scales 0, inverse bf16(1)
-        const PadFill f0{out_fp4, (int)code_bytes, 0u}, f1{out_scales, (int)scale_bytes, 0u},
-            f2{out_inv, 2, 0x3F803F80u};
-        for (int q = blockIdx.x; q < G * fparts; q += gridDim.x)
-            fill_group_padding(q / fparts, q % fparts, fparts, pad, R_max, row_offsets, src_info, status,
-                               f0, f1, f2);
-    }
     bulk_wait_all();                // every copy of this thread has landed
 }
 
@@ -486,9 +490,10 @@ inline int launch_nvfp4_staged(int grid, const uint16_t *x, int H, const int32_t
     const int G = L->E + L->fused_shared;
     const int R_max = layout_rows(L);
     const int pad = layout_padded(L) ? L->pad_multiple : 1;
-    return launch_pdl(ep_dispatch_nvfp4_staged_kernel, dim3(grid), dim3(threads), smem, st, x, L->T, H,
-                      L->K, L->E, L->fused_shared, G, R_max, early, write_meta, pad,
-                      fill_parts(L, threads), ids,
+    const int nfill = fill_ctas(L, threads);   // trailing CTAs for the padding rows
+    return launch_pdl(ep_dispatch_nvfp4_staged_kernel, dim3(grid + nfill), dim3(threads), smem, st, x,
+                      L->T, H, L->K, L->E, L->fused_shared, G, R_max, early, write_meta, pad,
+                      fill_parts(L, threads), grid, ids,
                       (const int32_t *)L->row_of, (const int32_t *)L->row_offsets,
                       (const int32_t *)L->status, out_fp4, out_scales, out_inv, scales_offsets,
                       L->src_info, L->expert_ids);
