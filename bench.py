@@ -132,18 +132,24 @@ class ClockSampler:
         except OSError:
             self.proc = None
 
-    def stop(self, t0: float, t1: float) -> dict:
+    def stop(self) -> None:
+        """End sampling; summary() then reads the samples of any time window."""
+        self.out = ""
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=10)
+            self.out, _ = self.proc.communicate(timeout=10)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
+            self.out, _ = self.proc.communicate()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         rows, reasons = [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.splitlines():
+        for line in self.out.splitlines():
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 10:
                 continue
@@ -418,7 +424,6 @@ def run_ours(args, cfg):
     torch.cuda.synchronize(dev)
     barrier(ws)
     t_host1 = time.time()
-    clocks = sampler.stop(t_host0, t_host1) if sampler else None
     per_step = np.array([e[0].elapsed_time(e[3]) for e in evs]) * 1e-3   # s
     total = float(per_step.sum())
     total_max = reduce_max(total, ws, dev)
@@ -511,6 +516,14 @@ def run_ours(args, cfg):
     static = static_routing_step(ep, dev, stream, flush_l2, nb)
     graphs = graph_replay(ep, dev, stream, flush_l2, nb)
     sweep = config_sweep(ep, dev, stream, flush_l2, min(nb, 100)) if not args.no_sweep else None
+    torch.cuda.synchronize(dev)
+    t_host2 = time.time()
+    clocks = clocks_run = None
+    if sampler:   # the timed steps alone, and every GPU phase of the run from them to the sweep
+        sampler.stop()
+        clocks = sampler.summary(t_host0, t_host1)
+        clocks_run = sampler.summary(t_host0, t_host2)
+        clocks_run["window"] = "the timed steps through the configs sweep (every GPU phase but e2e)"
 
     # ---- e2e through the public API with pinned host buffers ----
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
@@ -639,6 +652,7 @@ def run_ours(args, cfg):
                         "combine through the C ABI, dispatched rows + metadata + combined output -> host"},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
+        "clocks_run": clocks_run,
         "rows": R,
     }
     if ws == 1 and not args.no_cpu_baseline and sweep:
