@@ -9,7 +9,8 @@
 // scale store per destination row).  The token row is read from HBM exactly once and stays in
 // registers: the row maximum is a block-wide reduction, the block maxima are per thread, the
 // E4M3 and E2M1 encodings are single hardware conversions, and the same bytes are then
-// stored to each of the token's K (+1 shared) rows.
+// stored to each of the token's K (+1 shared) rows.  The fused layout + NVFP4 calls run the
+// staged kernel described further down instead, where its shape allows.
 #include "ep_common.cuh"
 #include "ep_async.cuh"
 #include "ep_host.h"

@@ -7,7 +7,9 @@
 // (HybridEPDispatch.forward: the rows come out grouped by expert; an index of -1 routes
 // nowhere).
 //
-// Two launches on the caller's stream:
+// Up to 262,144 (token, slot) ids the whole layout is one launch of ep_layout_cluster_kernel on
+// a thread-block cluster (described before that kernel below).  Beyond that, and where the
+// cluster's shared-memory plan does not fit, two launches on the caller's stream:
 //   1. ep_layout_count_kernel: one CTA per tile of tokens builds the tile's expert histogram
 //      and partition token counts in shared memory and writes them to the workspace.  The
 //      CTA that finishes last (an atomic ticket, so no CTA ever waits on another) runs the
