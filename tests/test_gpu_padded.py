@@ -209,6 +209,12 @@ def test_padded_reuse_and_zero_tokens(ep):
     ep.dispatch_layout_routed(8, topk_ids=torch.empty(0, 2, dtype=torch.int32, device="cuda"),
                               fused_shared=True, pad_multiple=4, out=L0)
     assert ep.read_status(L0) == 0 and L0.row_offsets.cpu().tolist() == [0] * 10
+    # the padded layout + NVFP4 call with no tokens: an empty layout, scales_offsets all 0
+    L1, (_, _, _, so) = ep.dispatch_layout_padded_nvfp4(
+        torch.empty(0, 2, dtype=torch.int32, device="cuda"),
+        torch.empty(0, 256, dtype=torch.bfloat16, device="cuda"), 8, fused_shared=True, pad_multiple=4)
+    assert ep.read_status(L1) == 0 and L1.row_offsets.cpu().tolist() == [0] * 10
+    assert so.cpu().tolist() == [0] * 10
 
 
 EDGE = [  # T, K, E, S, P, pad, case
