@@ -979,7 +979,7 @@ def static_routing_step(ep, dev, stream, flush_l2, n_steps: int) -> dict:
 
 ONLY_OPS = ("layout", "layout_noalloc", "dispatch_layout_nvfp4", "dispatch_nvfp4", "dispatch_bf16",
             "dispatch_fp8", "combine", "combine_bwd", "dispatch_bwd", "indices_to_multihot",
-            "routing_map_layout")
+            "routing_map_layout", "dispatch_nvfp4_padded", "dispatch_layout_padded_nvfp4")
 
 
 def run_only(args, cfg):
@@ -1003,21 +1003,32 @@ def run_only(args, cfg):
     def randn(*shape):
         return torch.randn(*shape, device=dev, generator=gen).to(torch.bfloat16)
 
-    L = ep.Layout(T, K, E, P, bool(S), device=dev)
-    ep.dispatch_layout(ids, E, P, C, bool(S), out=L, stream=stream)
     op = args.only
+    padded = op in ("dispatch_nvfp4_padded", "dispatch_layout_padded_nvfp4")
+    pad = args.pad if padded else 1
+    L = ep.Layout(T, K, E, P, bool(S), device=dev, pad_multiple=pad)
+    if padded:
+        ep.dispatch_layout_routed(E, topk_ids=ids, n_parts=P, capacity=C, fused_shared=bool(S),
+                                  pad_multiple=pad, out=L, stream=stream)
+        R_max = L.R_max
+    else:
+        ep.dispatch_layout(ids, E, P, C, bool(S), out=L, stream=stream)
     if op == "layout":
         fn = lambda: ep.dispatch_layout(ids, E, P, C, bool(S), out=L, stream=stream)
     elif op == "layout_noalloc":
         fn = lambda: ep.dispatch_layout_noalloc(ids, E, P, C, bool(S), out=L, stream=stream)
-    elif op in ("dispatch_layout_nvfp4", "dispatch_nvfp4"):
+    elif op in ("dispatch_layout_nvfp4", "dispatch_nvfp4", "dispatch_nvfp4_padded",
+                "dispatch_layout_padded_nvfp4"):
         x = randn(T, H)
         rows = (torch.empty(R_max, H // 2, dtype=torch.uint8, device=dev),
                 torch.empty(R_max, H // 16, dtype=torch.uint8, device=dev),
                 torch.empty(R_max, dtype=torch.bfloat16, device=dev),
                 torch.empty(E + S + 1, dtype=torch.int32, device=dev))
-        if op == "dispatch_nvfp4":
+        if op in ("dispatch_nvfp4", "dispatch_nvfp4_padded"):
             fn = lambda: ep.dispatch_nvfp4(x, L, out=rows, stream=stream)
+        elif op == "dispatch_layout_padded_nvfp4":
+            fn = lambda: ep.dispatch_layout_padded_nvfp4(ids, x, E, P, C, bool(S), pad, None, out_layout=L,
+                                                         out=rows, stream=stream)
         else:
             fn = lambda: ep.dispatch_layout_nvfp4(ids, x, E, P, C, bool(S), out_layout=L, out=rows,
                                                   stream=stream)
@@ -1068,10 +1079,14 @@ def run_only(args, cfg):
     torch.cuda.synchronize(dev)
     sec = float(np.mean([a.elapsed_time(b) for a, b in evs])) * 1e-3
     R = int(L.row_offsets[L.G].item())
-    ab = algorithmic_bytes(cfg, R)
-    key = {"layout_noalloc": "layout", "dispatch_layout_nvfp4": None}.get(op, op)
-    nbytes = ab["layout"] + ab["dispatch_nvfp4"] if key is None else ab.get(key)
-    line = {"only": op, "workload": cfg.name, "T": T, "hidden": H, "rows": R, "steps": args.steps,
+    ab = padded_bytes(cfg, R) if padded else algorithmic_bytes(cfg, R)
+    key = {"layout_noalloc": "layout", "dispatch_nvfp4_padded": "dispatch_nvfp4"}.get(op, op)
+    if op in ("dispatch_layout_nvfp4", "dispatch_layout_padded_nvfp4"):
+        nbytes = ab["layout"] + ab["dispatch_nvfp4"]
+    else:
+        nbytes = ab.get(key)
+    line = {"only": op, "workload": cfg.name, "T": T, "hidden": H, "pad_multiple": pad, "rows": R,
+            "steps": args.steps,
             "warmup": args.warmup, "us": sec * 1e6, "algorithmic_bytes": nbytes,
             "GB/s": nbytes / sec / 1e9 if nbytes else None}
     print(json.dumps(line), flush=True)
@@ -1094,6 +1109,9 @@ def main():
                     help="run one library call alone on --config (for profiling) and print its time")
     ap.add_argument("--tokens", type=int, default=None,
                     help="with --only: the workload's recipe at this many tokens")
+    ap.add_argument("--pad", type=int, default=128,
+                    help="with --only dispatch_nvfp4_padded / dispatch_layout_padded_nvfp4: rows per "
+                         "group multiple")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
