@@ -10,7 +10,9 @@ Prints one JSON line.  `value` is tokens/s over all ranks (independent replicas,
 the path does not shard), `e2e` the same metric through the C ABI with pinned host buffers
 (host->device inputs and device->host results inside the timed region), `roofline` the
 dominant kernel (combine) against the measured HBM copy bandwidth, `cpu_baseline` the CPU
-oracle on a bounded sample.
+oracle on a bounded sample.  `configs_sweep` runs the step on every workload recipe, with
+the other calls each workload names, its end-to-end figure from pinned host buffers and the
+oracle timed per op.
 
     python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference]
 """
@@ -682,7 +684,8 @@ def pipelined_e2e(ep, cfg: W.Config, dev, hx, hids, hprobs, hy, n_steps: int, re
     than one each, the host link being the limit, so one each is the default.  Checks that the
     last step's host output equals ref_out."""
     import torch
-    T, H, E, K, S, P, C = cfg.T, cfg.H, cfg.E, cfg.K, cfg.S, cfg.P, cfg.capacity
+    T, H, E, K, S, P = cfg.T, cfg.H, cfg.E, cfg.K, cfg.S, cfg.P
+    C = cfg.rerun_C if cfg.rerun_C else cfg.capacity
     R_max = W.r_max(cfg)
 
     def slices(n_rows, n):
@@ -772,7 +775,16 @@ def config_sweep(ep, dev, stream, flush_l2, n_steps: int) -> list:
     event at its start and end, then the two calls timed in a second pass with an event between.
     Routing comes from the seeded recipes; x and the expert outputs are seeded device draws
     (N(0,1) bf16): the kernels' work does not depend on their values.  The large microbatch runs
-    at its rerun capacity, where nothing overflows."""
+    at its rerun capacity, where nothing overflows.
+
+    Each entry also carries:
+      ops  -- the other calls the workload names, each timed alone on the same layout (L2
+              flushed before each call, events around it): the BF16 dispatch (tiny, Mixtral-like),
+              both backward passes (Qwen3-like), and for the large microbatch the fused call at
+              its first capacity, which must raise the overflow flag;
+      e2e  -- the step through the C ABI from pinned host buffers, pipelined as the headline
+              e2e figure is (pipelined_e2e): host->device copies of x, ids, probs and the
+              expert outputs, the two calls, device->host copies of every result."""
     import torch
     peak, _ = load_peaks()
     res = []
@@ -837,10 +849,95 @@ def config_sweep(ep, dev, stream, flush_l2, n_steps: int) -> list:
                                       "combine": comb_b / t[1] / 1e9 / peak,
                                       "step": (disp_b + comb_b) / t[2] / 1e9 / peak},
             "frac_of_8TB/s": {"step": (disp_b + comb_b) / t[2] / 8e12},
+            "ops": sweep_ops(ep, cfg, dev, stream, flush_l2, max(3, n_steps // 2), ids, probs, x, y, L,
+                             R, ab, peak),
+            "e2e": sweep_e2e(ep, cfg, dev, ids_h, probs_h, x, y, out),
         })
         del x, y, rows, out, L
         torch.cuda.empty_cache()
     return res
+
+
+def sweep_ops(ep, cfg: W.Config, dev, stream, flush_l2, n: int, ids, probs, x, y, L, R: int, ab: dict,
+              peak: float) -> dict:
+    """The calls a workload names besides the benchmark step, each timed alone on the step's
+    layout and inputs: mean of n launches, L2 flushed before each, events around each."""
+    import torch
+    T, H, E, K, S, P = cfg.T, cfg.H, cfg.E, cfg.K, cfg.S, cfg.P
+    R_max = W.r_max(cfg)
+    fns, status_of = {}, {}
+    if cfg.name in ("tiny", "mixtral"):
+        rows_bf16 = torch.empty(R_max, H, dtype=torch.bfloat16, device=dev)
+        fns["dispatch_bf16"] = lambda: ep.dispatch_bf16(x, L, out=rows_bf16, stream=stream)
+    if cfg.name == "qwen3":
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(9100 + cfg.index)
+        g_out = torch.randn(T, H, device=dev, generator=gen).to(torch.bfloat16)
+        g_rows = torch.empty(R_max, H, dtype=torch.bfloat16, device=dev)
+        g_probs = torch.empty(T, K, dtype=torch.float32, device=dev)
+        g_x = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        fns["combine_bwd"] = lambda: ep.combine_bwd(g_out, y, probs, L, out=(g_rows, g_probs), stream=stream)
+        fns["dispatch_bwd"] = lambda: ep.dispatch_bwd(y, L, out=g_x, stream=stream)
+    if cfg.rerun_C:
+        # the first capacity: the layout flags the overflow and the dispatch writes no row
+        Lo = ep.Layout(T, K, E, P, bool(S), device=dev)
+        o_rows = (torch.empty(R_max, H // 2, dtype=torch.uint8, device=dev),
+                  torch.empty(R_max, H // 16, dtype=torch.uint8, device=dev),
+                  torch.empty(R_max, dtype=torch.bfloat16, device=dev),
+                  torch.empty(E + S + 1, dtype=torch.int32, device=dev))
+        name = f"dispatch_layout_nvfp4 (capacity {cfg.capacity}, overflow)"
+        fns[name] = lambda: ep.dispatch_layout_nvfp4(ids, x, E, P, cfg.capacity, bool(S), out_layout=Lo,
+                                                     out=o_rows, stream=stream)
+        status_of[name] = Lo
+    res = {}
+    for name, fn in fns.items():
+        for _ in range(3):
+            flush_l2()
+            fn()
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(n)]
+        for a, b in pairs:
+            flush_l2()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        sec = float(np.mean([a.elapsed_time(b) for a, b in pairs])) * 1e-3
+        entry = {"us": sec * 1e6, "tokens/s": T / sec, "launches": n}
+        if name in status_of:
+            st = ep.read_status(status_of[name])
+            if not st & ep.STATUS_OVERFLOW:
+                raise RuntimeError(f"{cfg.name}: no overflow flag at capacity {cfg.capacity}")
+            entry["status"] = st
+        else:
+            entry["algorithmic_bytes"] = ab[name]
+            entry["frac_of_measured_peak"] = ab[name] / sec / 1e9 / peak
+        res[name] = entry
+    return res
+
+
+def sweep_e2e(ep, cfg: W.Config, dev, ids_h, probs_h, x, y, ref_out) -> dict:
+    """The step end to end through the C ABI from pinned host buffers (pipelined_e2e), on the
+    workload's own inputs; about 0.3 s of host-link time, 3 to 20 steps."""
+    import torch
+    hx = x.view(torch.int16).cpu().pin_memory()
+    hy = y.view(torch.int16).cpu().pin_memory()
+    hids = torch.from_numpy(ids_h).pin_memory()
+    hprobs = torch.from_numpy(probs_h).pin_memory()
+    T, H, E, K, S, P = cfg.T, cfg.H, cfg.E, cfg.K, cfg.S, cfg.P
+    R_max = W.r_max(cfg)
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hids, hprobs, hy))
+    # the copies pipelined_e2e makes back: dispatched rows (codes, scales, inverse scales),
+    # scales offsets, combined output and the layout's row_offsets, expert_ids, src_info, status
+    Ls = ep.Layout(T, K, E, P, bool(S), device=dev)
+    d2h = (R_max * (H // 2 + H // 16 + 2) + 4 * (E + S + 1) + 2 * T * H
+           + sum(t.numel() * t.element_size() for t in (Ls.row_offsets, Ls.expert_ids, Ls.src_info, Ls.status)))
+    del Ls
+    n = int(max(3, min(20, 0.3 / max(h2d / 2e11, 1e-6))))
+    sec = pipelined_e2e(ep, cfg, dev, hx, hids, hprobs, hy, n, ref_out)
+    return {"tokens/s": T * n / sec, "us_per_step": sec / n * 1e6, "steps": n,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "host_link_GB/s": (h2d + d2h) * n / sec / 1e9}
 
 
 def graph_replay(ep, dev, stream, flush_l2, n_steps: int) -> list:

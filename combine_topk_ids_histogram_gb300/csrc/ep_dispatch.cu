@@ -149,14 +149,27 @@ ep_dispatch_nvfp4_kernel(const uint16_t *__restrict__ x, int T, int H, int K, in
     }
 }
 
-constexpr int kBf16Chunks = 4;   // 16-byte chunks of a row one thread holds at a time
+// BF16 dispatch: each CTA copies a run of up to kBf16Tokens consecutive tokens, as many as fill
+// kBf16Chunks 16-byte chunks per thread (one token above H = 4096, two at H = 4096, four at
+// H = 2048 and below), so a short row does not pay a CTA's start-up and row-index wait alone.  The
+// run's rows are contiguous in x: chunk c of the run is chunk c mod H/8 of its token c div H/8.
+// Every chunk a thread holds is requested before the first is stored, then stored to each of
+// its token's K (+1) rows.
+constexpr int kBf16Chunks = 4;   // 16-byte chunks of the run one thread holds at a time
+constexpr int kBf16Tokens = 4;   // most tokens one CTA copies
+constexpr int kBf16Threads = 256;
 
-__global__ void __launch_bounds__(256)
+inline int bf16_tokens_per_cta(int H) {
+    const int per = kBf16Chunks * kBf16Threads / (H / 8);
+    return per < 1 ? 1 : (per > kBf16Tokens ? kBf16Tokens : per);
+}
+
+__global__ void __launch_bounds__(kBf16Threads)
 ep_dispatch_bf16_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int E, int S, int R_max,
-                        int nfill, int fparts, int pad, const int32_t *__restrict__ row_of,
+                        int nfill, int fparts, int pad, int tpc, const int32_t *__restrict__ row_of,
                         const int32_t *__restrict__ row_offsets, const int32_t *__restrict__ src_info,
                         const int32_t *__restrict__ status, uint16_t *__restrict__ out, PadFill f0) {
-    __shared__ int s_rows[kMaxRowsPerToken];
+    __shared__ int s_rows[kBf16Tokens][kMaxRowsPerToken];
     pdl_wait();
     if (cta_status(status)) return;
     if ((int)blockIdx.x < nfill) {   // leading CTAs of a padded layout: a group's padding rows
@@ -166,30 +179,33 @@ ep_dispatch_bf16_kernel(const uint16_t *__restrict__ x, int T, int H, int K, int
         return;
     }
     const int tid = threadIdx.x;
-    const int t = blockIdx.x - nfill;
+    const int t0 = (blockIdx.x - nfill) * tpc;
+    const int nt = min(tpc, T - t0);   // tokens of this run (the last run may be shorter)
     const int nrows = K + S;
-    if (tid < K) s_rows[tid] = row_of[(size_t)t * K + tid];
-    else if (tid == K && S) s_rows[K] = row_offsets[E] + t;
+    for (int j = tid; j < nt * nrows; j += blockDim.x) {
+        const int g = j / nrows, k = j - g * nrows;
+        s_rows[g][k] = k < K ? row_of[(size_t)(t0 + g) * K + k] : row_offsets[E] + t0 + g;
+    }
     __syncthreads();
-    const int nv = H / 8;
-    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
-    // the row's 16-byte chunks of this thread are all requested before the first is stored
-    // (up to kBf16Chunks per thread at a time)
-    for (int c0 = tid; c0 < nv; c0 += kBf16Chunks * blockDim.x) {
+    const int nv = H / 8;          // 16-byte chunks of one token's row
+    const int nrun = nt * nv;      // of the run
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t0 * H);
+    for (int c0 = tid; c0 < nrun; c0 += kBf16Chunks * blockDim.x) {
         uint4 d[kBf16Chunks];
 #pragma unroll
         for (int i = 0; i < kBf16Chunks; ++i) {
             const int c = c0 + i * blockDim.x;
-            if (c < nv) d[i] = ld_stream(src + c);
+            if (c < nrun) d[i] = ld_stream(src + c);
         }
-        for (int k = 0; k < nrows; ++k) {
-            const int r = s_rows[k];
-            if (!row_ok(r, R_max, status)) continue;
-            uint16_t *dst = out + (size_t)r * H;
 #pragma unroll
-            for (int i = 0; i < kBf16Chunks; ++i) {
-                const int c = c0 + i * blockDim.x;
-                if (c < nv) st_stream(dst + (size_t)c * 8, d[i]);
+        for (int i = 0; i < kBf16Chunks; ++i) {
+            const int c = c0 + i * blockDim.x;
+            if (c >= nrun) continue;
+            const int g = c / nv, cc = c - g * nv;
+            for (int k = 0; k < nrows; ++k) {
+                const int r = s_rows[g][k];
+                if (!row_ok(r, R_max, status)) continue;
+                st_stream(out + (size_t)r * H + (size_t)cc * 8, d[i]);
             }
         }
     }
@@ -653,12 +669,14 @@ extern "C" int ep_dispatch_bf16(const uint16_t *input_tokens, int hidden_size, c
     if (L->T > 0 && (!input_tokens || !out)) return EP_ERR_INVALID_ARG;
     if ((input_tokens && !aligned16(input_tokens)) || (out && !aligned16(out))) return EP_ERR_INVALID_ARG;
     if (L->T == 0) return EP_OK;
-    const int nfill = fill_ctas(L, 256);   // padding rows: zeros
-    return launch_pdl(ep_dispatch_bf16_kernel, dim3(L->T + nfill), dim3(256), 0, as_stream(stream),
-                      input_tokens, L->T, H, L->K, L->E, L->fused_shared, layout_rows(L), nfill,
-                      fill_parts(L, 256), L->pad_multiple, (const int32_t *)L->row_of,
-                      (const int32_t *)L->row_offsets, (const int32_t *)L->src_info,
-                      (const int32_t *)L->status, out, PadFill{out, 2 * H, 0u});
+    const int nfill = fill_ctas(L, kBf16Threads);   // padding rows: zeros
+    const int tpc = bf16_tokens_per_cta(H);
+    return launch_pdl(ep_dispatch_bf16_kernel, dim3((L->T + tpc - 1) / tpc + nfill), dim3(kBf16Threads), 0,
+                      as_stream(stream), input_tokens, L->T, H, L->K, L->E, L->fused_shared,
+                      layout_rows(L), nfill, fill_parts(L, kBf16Threads), L->pad_multiple, tpc,
+                      (const int32_t *)L->row_of, (const int32_t *)L->row_offsets,
+                      (const int32_t *)L->src_info, (const int32_t *)L->status, out,
+                      PadFill{out, 2 * H, 0u});
 }
 
 extern "C" int ep_dispatch_fp8(const uint16_t *input_tokens, int hidden_size, const ep_layout_t *L,
