@@ -234,6 +234,7 @@ using namespace ep;
 
 extern "C" int ep_combine(const uint16_t *expert_out, const float *probs, int hidden_size,
                           const ep_layout_t *L, uint16_t *out, void *stream) {
+    EP_NVTX_RANGE("ep_combine");
     const int H = hidden_size;
     if (!layout_ok(L) || !hidden_ok(H)) return EP_ERR_INVALID_ARG;
     if (L->T > 0 && (!expert_out || !probs || !out)) return EP_ERR_INVALID_ARG;
@@ -246,6 +247,7 @@ extern "C" int ep_combine(const uint16_t *expert_out, const float *probs, int hi
 
 extern "C" int ep_dispatch_bwd(const uint16_t *grad_rows, int hidden_size, const ep_layout_t *L,
                                uint16_t *grad_input, void *stream) {
+    EP_NVTX_RANGE("ep_dispatch_bwd");
     const int H = hidden_size;
     if (!layout_ok(L) || !hidden_ok(H)) return EP_ERR_INVALID_ARG;
     if (L->T > 0 && (!grad_rows || !grad_input)) return EP_ERR_INVALID_ARG;
@@ -258,6 +260,7 @@ extern "C" int ep_dispatch_bwd(const uint16_t *grad_rows, int hidden_size, const
 extern "C" int ep_combine_bwd(const uint16_t *grad_out, const uint16_t *expert_out, const float *probs,
                               int hidden_size, const ep_layout_t *L, uint16_t *grad_expert_out,
                               float *grad_probs, void *stream) {
+    EP_NVTX_RANGE("ep_combine_bwd");
     const int H = hidden_size;
     if (!layout_ok(L) || !hidden_ok(H)) return EP_ERR_INVALID_ARG;
     if (L->T > 0 && (!grad_out || !expert_out || !probs || !grad_expert_out || !grad_probs))

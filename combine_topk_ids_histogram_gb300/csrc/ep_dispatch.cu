@@ -586,6 +586,7 @@ int launch_nvfp4(const uint16_t *input_tokens, int H, const ep_layout_t *L, uint
 extern "C" int ep_dispatch_nvfp4(const uint16_t *input_tokens, int hidden_size, const ep_layout_t *L,
                                  uint8_t *out_fp4, uint8_t *out_scales, uint16_t *out_rowwise_inv_scale,
                                  int32_t *scales_offsets, void *stream) {
+    EP_NVTX_RANGE("ep_dispatch_nvfp4");
     return launch_nvfp4(input_tokens, hidden_size, L, out_fp4, out_scales, out_rowwise_inv_scale,
                         scales_offsets, 0, as_stream(stream));
 }
@@ -596,6 +597,7 @@ extern "C" int ep_dispatch_layout_nvfp4(const int32_t *topk_ids, int T, int K, i
                                         ep_layout_t *L, uint8_t *out_fp4, uint8_t *out_scales,
                                         uint16_t *out_rowwise_inv_scale, int32_t *scales_offsets,
                                         void *stream) {
+    EP_NVTX_RANGE("ep_dispatch_layout_nvfp4");
     const int H = hidden_size;
     if (!hidden_ok(H) || H / 16 > 1024) return EP_ERR_INVALID_ARG;
     if ((T > 0 && (!input_tokens || !out_fp4 || !out_scales || !out_rowwise_inv_scale)) ||
@@ -637,6 +639,7 @@ extern "C" int ep_dispatch_layout_padded_nvfp4(const int32_t *topk_ids, int T, i
                                                ep_layout_t *L, uint8_t *out_fp4, uint8_t *out_scales,
                                                uint16_t *out_rowwise_inv_scale, int32_t *scales_offsets,
                                                void *stream) {
+    EP_NVTX_RANGE("ep_dispatch_layout_padded_nvfp4");
     const int H = hidden_size;
     if (!hidden_ok(H) || H / 16 > 1024) return EP_ERR_INVALID_ARG;
     if ((T > 0 && (!input_tokens || !out_fp4 || !out_scales || !out_rowwise_inv_scale)) ||
@@ -664,6 +667,7 @@ extern "C" int ep_dispatch_layout_padded_nvfp4(const int32_t *topk_ids, int T, i
 
 extern "C" int ep_dispatch_bf16(const uint16_t *input_tokens, int hidden_size, const ep_layout_t *L,
                                 uint16_t *out, void *stream) {
+    EP_NVTX_RANGE("ep_dispatch_bf16");
     const int H = hidden_size;
     if (!layout_ok(L) || !hidden_ok(H)) return EP_ERR_INVALID_ARG;
     if (L->T > 0 && (!input_tokens || !out)) return EP_ERR_INVALID_ARG;
@@ -681,6 +685,7 @@ extern "C" int ep_dispatch_bf16(const uint16_t *input_tokens, int hidden_size, c
 
 extern "C" int ep_dispatch_fp8(const uint16_t *input_tokens, int hidden_size, const ep_layout_t *L,
                                uint8_t *out_fp8, float *out_scales, void *stream) {
+    EP_NVTX_RANGE("ep_dispatch_fp8");
     const int H = hidden_size;
     if (!layout_ok(L) || !hidden_ok(H) || H % kFp8Block != 0) return EP_ERR_INVALID_ARG;
     if (L->T > 0 && (!input_tokens || !out_fp8 || !out_scales)) return EP_ERR_INVALID_ARG;

@@ -2,8 +2,10 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include <mutex>
 #include <utility>
@@ -11,6 +13,31 @@
 #include "ep.h"
 
 namespace ep {
+
+// Optional NVTX range around each entry point, named after it, so that a profiler can select an
+// op's kernels by range (ncu --nvtx --nvtx-include "ep_combine/", or a timeline tool).  On when
+// the environment variable EP_GB300_NVTX is set to anything but "0" when the library first
+// checks it; otherwise an entry point pays one test of a cached flag.  The header-only NVTX
+// API does nothing unless a profiler is attached.
+inline bool nvtx_enabled() {
+    static const bool on = [] {
+        const char *v = getenv("EP_GB300_NVTX");
+        return v != nullptr && v[0] != '\0' && !(v[0] == '0' && v[1] == '\0');
+    }();
+    return on;
+}
+struct NvtxScope {
+    bool on;
+    explicit NvtxScope(const char *name) : on(nvtx_enabled()) {
+        if (on) nvtxRangePushA(name);
+    }
+    ~NvtxScope() {
+        if (on) nvtxRangePop();
+    }
+    NvtxScope(const NvtxScope &) = delete;
+    NvtxScope &operator=(const NvtxScope &) = delete;
+};
+#define EP_NVTX_RANGE(name) ::ep::NvtxScope ep_nvtx_range_(name)
 
 constexpr int kMaxK = 32;
 constexpr int kMaxE = 1024;

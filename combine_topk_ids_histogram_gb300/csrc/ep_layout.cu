@@ -1001,6 +1001,7 @@ int launch_layout(const int32_t *topk_ids, int T, int K, int E, int P, int capac
 extern "C" int ep_dispatch_layout(const int32_t *topk_ids, int T, int K, int n_experts,
                                   int n_parts, int capacity, int fused_shared, ep_layout_t *L,
                                   void *stream) {
+    EP_NVTX_RANGE("ep_dispatch_layout");
     return launch_layout(topk_ids, T, K, n_experts, n_parts, capacity, fused_shared, 1, 0, L,
                          as_stream(stream), nullptr);
 }
@@ -1019,6 +1020,7 @@ extern "C" int ep_dispatch_layout_routed(const int32_t *topk_ids, const uint8_t 
                                          int pad_multiple, int num_permuted_tokens,
                                          int32_t *map_topk_ids, float *map_topk_probs,
                                          ep_layout_t *L, void *stream) {
+    EP_NVTX_RANGE("ep_dispatch_layout_routed");
     cudaStream_t st = as_stream(stream);
     const int32_t *ids = topk_ids;
     if (routing_map) {   // the map takes precedence: convert it, then lay out its compact form
@@ -1035,6 +1037,7 @@ extern "C" int ep_dispatch_layout_routed(const int32_t *topk_ids, const uint8_t 
 }
 
 extern "C" int ep_read_status(const ep_layout_t *L, void *stream, int32_t *host_status) {
+    EP_NVTX_RANGE("ep_read_status");
     if (!L || !L->status || !host_status) return EP_ERR_INVALID_ARG;
     cudaStream_t st = as_stream(stream);
     int32_t v = 0;
@@ -1114,6 +1117,7 @@ int noalloc_workspace(void **out) {
 extern "C" int ep_dispatch_layout_noalloc(const int32_t *topk_ids, int T, int K, int n_experts,
                                           int n_parts, int capacity, int fused_shared,
                                           ep_layout_t *L, void *stream) {
+    EP_NVTX_RANGE("ep_dispatch_layout_noalloc");
     const int E = n_experts, P = n_parts, S = fused_shared;
     if (!L || !sizes_ok(T, K, E, S)) return EP_ERR_INVALID_ARG;
     if (P < 1 || P > E || E % P != 0 || capacity < 0) return EP_ERR_INVALID_ARG;

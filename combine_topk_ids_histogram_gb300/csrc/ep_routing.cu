@@ -238,6 +238,7 @@ using namespace ep;
 extern "C" int ep_routing_map_to_topk(const uint8_t *routing_map, const float *dense_probs, int T,
                                       int n_experts, int K, int32_t *topk_ids, float *topk_probs,
                                       void *stream) {
+    EP_NVTX_RANGE("ep_routing_map_to_topk");
     return launch_map_to_topk(routing_map, dense_probs, T, n_experts, K, topk_ids, topk_probs,
                               as_stream(stream));
 }
@@ -245,6 +246,7 @@ extern "C" int ep_routing_map_to_topk(const uint8_t *routing_map, const float *d
 extern "C" int ep_indices_to_multihot(const int32_t *topk_ids, const float *topk_probs, int T, int K,
                                       int n_experts, uint8_t *routing_map, float *dense_probs,
                                       void *stream) {
+    EP_NVTX_RANGE("ep_indices_to_multihot");
     const int E = n_experts;
     if (T < 0 || T > kMaxT || E < 1 || E > kMaxE || K < 1 || K > kMaxK) return EP_ERR_INVALID_ARG;
     if (T > 0 && (!topk_ids || !routing_map)) return EP_ERR_INVALID_ARG;

@@ -33,6 +33,11 @@
  * Limits.  0 <= T <= 2^24, 1 <= K <= 32, 1 <= E <= 1024 (K may exceed E: a token may
  *   name an expert in several slots), 1 <= P <= E with E % P == 0,
  *   C >= 0, R_max < 2^31; H % 16 == 0 and 16 <= H <= 32768.
+ * Profiling.  With the environment variable EP_GB300_NVTX set to anything but "0" when the
+ *   library first checks it, each entry point that enqueues work (and ep_read_status) wraps
+ *   itself in an NVTX range named after it, so a profiler can select an op's kernels by range
+ *   (for example ncu --nvtx --nvtx-include "ep_combine/").  Off by default; results are the same
+ *   either way.
  */
 #ifndef EP_GB300_H
 #define EP_GB300_H
