@@ -517,7 +517,10 @@ def run_ours(args, cfg):
     R_pad = int(Lp.row_offsets[Lp.G].item())
     static = static_routing_step(ep, dev, stream, flush_l2, nb)
     graphs = graph_replay(ep, dev, stream, flush_l2, nb)
-    sweep = config_sweep(ep, dev, stream, flush_l2, min(nb, 100)) if not args.no_sweep else None
+    # the per-workload sweep (with its pinned-host e2e legs) runs on one GPU only: a run over
+    # several GPUs measures the headline step, whose replicas are what scale
+    sweep = (config_sweep(ep, dev, stream, flush_l2, min(nb, 100))
+             if not args.no_sweep and ws == 1 else None)
     torch.cuda.synchronize(dev)
     t_host2 = time.time()
     clocks = clocks_run = None
