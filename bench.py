@@ -864,11 +864,15 @@ def config_sweep(ep, dev, stream, flush_l2, n_steps: int) -> list:
 def sweep_ops(ep, cfg: W.Config, dev, stream, flush_l2, n: int, ids, probs, x, y, L, R: int, ab: dict,
               peak: float) -> dict:
     """The calls a workload names besides the benchmark step, each timed alone on the step's
-    layout and inputs: mean of n launches, L2 flushed before each, events around each."""
+    layout and inputs: mean of n launches, L2 flushed before each, events around each.  Combine
+    is also timed alone: in the step it carries the write-back of the dispatch's rows that are
+    still dirty in L2 when it starts, alone it does not."""
     import torch
     T, H, E, K, S, P = cfg.T, cfg.H, cfg.E, cfg.K, cfg.S, cfg.P
     R_max = W.r_max(cfg)
     fns, status_of = {}, {}
+    out_alone = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    fns["combine"] = lambda: ep.combine(y, probs, L, out=out_alone, stream=stream)
     if cfg.name in ("tiny", "mixtral"):
         rows_bf16 = torch.empty(R_max, H, dtype=torch.bfloat16, device=dev)
         fns["dispatch_bf16"] = lambda: ep.dispatch_bf16(x, L, out=rows_bf16, stream=stream)
